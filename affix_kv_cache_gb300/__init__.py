@@ -1,0 +1,11 @@
+"""affix_kv_cache_gb300 -- the affix-cache attention hot path on GB300 (sm_103a).
+
+The compute path lives in libacache.so (hand-written CUDA, C ABI in include/acache.h);
+``_lib`` is its ctypes binding, ``workloads`` the seeded synthetic-input generator.
+Importing the package loads nothing; the library is loaded on first use and a missing
+library is an error.
+"""
+from ._lib import (AcacheError, AttnDesc, attn_desc, acache_build_slot_maps,  # noqa: F401
+                   acache_gather_slots, acache_probe_scores, acache_probe_workspace_bytes,
+                   acache_slot_attention, acache_topk_anchors, acache_write_slots, lib,
+                   status_string, version)

@@ -1,0 +1,169 @@
+"""ctypes binding of libacache.so (include/acache.h).
+
+Argument marshalling only: every function takes torch tensors (device memory) or plain
+integers, passes their device pointers, sizes and the current CUDA stream to the C entry
+point of the same name, and raises AcacheError on a non-zero status.  No step of the
+path runs here, and there is no fallback: if the library is missing, importing this
+module's functions fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libacache.so")
+
+ACACHE_OK = 0
+ACACHE_ERR_INVALID_ARG = -1
+ACACHE_ERR_UNSUPPORTED = -2
+ACACHE_ERR_CUDA = -3
+ACACHE_ERR_WORKSPACE = -4
+ACACHE_ERR_TIMEOUT = -5
+ACACHE_F32 = 0
+ACACHE_BF16 = 1
+DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
+
+EXPORTS = ("acache_status_string", "acache_version", "acache_probe_workspace_bytes",
+           "acache_probe_scores", "acache_topk_anchors", "acache_build_slot_maps",
+           "acache_write_slots", "acache_slot_attention", "acache_gather_slots")
+
+
+class AcacheError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} returned {status} ({status_string(status)})")
+        self.status = status
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("dtype", ctypes.c_int32)]
+
+
+def attn_desc(hq: int, hkv: int, d: int, scale: float, dtype) -> AttnDesc:
+    if isinstance(dtype, torch.dtype):
+        dtype = {torch.float32: ACACHE_F32, torch.bfloat16: ACACHE_BF16}[dtype]
+    elif isinstance(dtype, str):
+        dtype = {"f32": ACACHE_F32, "bf16": ACACHE_BF16}[dtype]
+    return AttnDesc(hq, hkv, d, scale, dtype)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libacache.so (built by __graft_entry__.build() or build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libacache.so is not built ({LIB_PATH} missing); "
+                               "run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        D = ctypes.POINTER(AttnDesc)
+        sig = {
+            "acache_status_string": (ctypes.c_char_p, [I]),
+            "acache_version": (I, []),
+            "acache_probe_workspace_bytes": (S, [D, I, I, I, I]),
+            "acache_probe_scores": (I, [D, I, I, I, I, P, I, P, P, P, P, P, P, P, P, S, P, P]),
+            "acache_topk_anchors": (I, [P, I, I, I, P, P, P]),
+            "acache_build_slot_maps": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
+            "acache_write_slots": (I, [D, I, I, P, P, P, P, P, I64, I64, P, P]),
+            "acache_slot_attention": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
+            "acache_gather_slots": (I, [D, I, I, P, P, P, I64, P, P, P, P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().acache_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(lib().acache_version())
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t or None
+    return t.data_ptr() or None
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return stream
+
+
+def _check(fn, status):
+    if status != ACACHE_OK:
+        raise AcacheError(fn, status)
+    return status
+
+
+def acache_probe_workspace_bytes(desc, batch, seq_len, affix_len, num_masked) -> int:
+    return int(lib().acache_probe_workspace_bytes(ctypes.byref(desc), batch, seq_len, affix_len,
+                                                  num_masked))
+
+
+def acache_probe_scores(desc, batch, seq_len, affix_begin, affix_len, masked_rows, num_masked,
+                        q, k_req, v_req, k_affix, v_affix, out, scores, workspace,
+                        workspace_bytes=None, dev_status=None, stream=None, check=True):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().acache_probe_scores(ctypes.byref(desc), batch, seq_len, affix_begin, affix_len,
+                                   _p(masked_rows), num_masked, _p(q), _p(k_req), _p(v_req),
+                                   _p(k_affix), _p(v_affix), _p(out), _p(scores), _p(workspace),
+                                   workspace_bytes, _p(dev_status), _stream(stream))
+    return _check("acache_probe_scores", st) if check else st
+
+
+def acache_topk_anchors(scores, batch, affix_len, k, anchors, dev_status=None, stream=None,
+                        check=True):
+    st = lib().acache_topk_anchors(_p(scores), batch, affix_len, k, _p(anchors), _p(dev_status),
+                                   _stream(stream))
+    return _check("acache_topk_anchors", st) if check else st
+
+
+def acache_build_slot_maps(batch, seq_len, affix_begin, affix_len, k, anchors, shared_slot,
+                           private_slots, write_pos, read_slot, dev_status=None, stream=None,
+                           check=True):
+    st = lib().acache_build_slot_maps(batch, seq_len, affix_begin, affix_len, k, _p(anchors),
+                                      _p(shared_slot), _p(private_slots), _p(write_pos),
+                                      _p(read_slot), _p(dev_status), _stream(stream))
+    return _check("acache_build_slot_maps", st) if check else st
+
+
+def acache_write_slots(desc, batch, rows, write_slot, k_new, v_new, k_cache, v_cache, num_slots,
+                       private_begin, dev_status=None, stream=None, check=True):
+    st = lib().acache_write_slots(ctypes.byref(desc), batch, rows, _p(write_slot), _p(k_new),
+                                  _p(v_new), _p(k_cache), _p(v_cache), num_slots, private_begin,
+                                  _p(dev_status), _stream(stream))
+    return _check("acache_write_slots", st) if check else st
+
+
+def acache_slot_attention(desc, batch, n_q, q, seq_len, read_slot, k_cache, v_cache, num_slots,
+                          out, dev_status=None, stream=None, check=True):
+    st = lib().acache_slot_attention(ctypes.byref(desc), batch, n_q, _p(q), seq_len, _p(read_slot),
+                                     _p(k_cache), _p(v_cache), num_slots, _p(out), _p(dev_status),
+                                     _stream(stream))
+    return _check("acache_slot_attention", st) if check else st
+
+
+def acache_gather_slots(desc, batch, seq_len, read_slot, k_cache, v_cache, num_slots, k_out,
+                        v_out, dev_status=None, stream=None, check=True):
+    st = lib().acache_gather_slots(ctypes.byref(desc), batch, seq_len, _p(read_slot), _p(k_cache),
+                                   _p(v_cache), num_slots, _p(k_out), _p(v_out), _p(dev_status),
+                                   _stream(stream))
+    return _check("acache_gather_slots", st) if check else st

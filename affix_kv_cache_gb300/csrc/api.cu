@@ -1,0 +1,236 @@
+// api.cu -- the C ABI of libacache.so: argument validation, workspace carving and kernel
+// dispatch.  Every entry point is declared and documented in include/acache.h.
+#include <math.h>
+
+#include "attn.cuh"
+#include "tc_attn.cuh"
+
+namespace acache {
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ACACHE_OK : ACACHE_ERR_CUDA;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Validates the attention descriptor; fills `out`.
+int check_desc(const acache_attn_desc* a, AttnArgs* out) {
+    if (!a) return ACACHE_ERR_INVALID_ARG;
+    if (a->num_q_heads <= 0 || a->num_kv_heads <= 0 || a->num_q_heads % a->num_kv_heads)
+        return ACACHE_ERR_INVALID_ARG;
+    if (!(a->scale == a->scale) || isinf(a->scale)) return ACACHE_ERR_INVALID_ARG;
+    if (a->dtype != ACACHE_F32 && a->dtype != ACACHE_BF16) return ACACHE_ERR_UNSUPPORTED;
+    if (a->head_dim != 64 && a->head_dim != 128) return ACACHE_ERR_UNSUPPORTED;
+    *out = AttnArgs{a->num_q_heads, a->num_kv_heads, a->head_dim, a->dtype, a->scale};
+    return ACACHE_OK;
+}
+
+size_t elem_bytes(int dtype) { return dtype == ACACHE_F32 ? 4 : 2; }
+
+struct ProbeWorkspace {
+    float* stat_m;
+    float* stat_l;
+    float* partial;
+    size_t bytes;
+};
+
+ProbeWorkspace carve_probe_ws(void* base, int64_t B, int64_t Hq, int64_t P, int64_t L) {
+    ProbeWorkspace w{};
+    const size_t st = align_up((size_t)(B * Hq * P) * sizeof(float));
+    const size_t pa = align_up((size_t)(B * Hq * L) * sizeof(float));
+    char* p = (char*)base;
+    w.stat_m = (float*)p;
+    w.stat_l = (float*)(p + st);
+    w.partial = (float*)(p + 2 * st);
+    w.bytes = 2 * st + pa;
+    return w;
+}
+
+// scores[b][j] += sum over heads h (ascending) of partial[b][h][j]
+__global__ void score_reduce_kernel(int B, int Hq, int L, const float* __restrict__ partial,
+                                    float* __restrict__ scores) {
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (int64_t)B * L) return;
+    const int64_t b = gid / L, j = gid % L;
+    float acc = scores[gid];
+    for (int h = 0; h < Hq; ++h) acc += partial[(b * Hq + h) * L + j];
+    scores[gid] = acc;
+}
+
+}  // namespace
+
+int launch_score_reduce(int B, int Hq, int L, const float* partial, float* scores,
+                        cudaStream_t stream) {
+    const int64_t n = (int64_t)B * L;
+    if (n == 0) return ACACHE_OK;
+    score_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(B, Hq, L, partial, scores);
+    return launch_status();
+}
+
+}  // namespace acache
+
+using namespace acache;
+
+extern "C" {
+
+const char* acache_status_string(int status) {
+    switch (status) {
+        case ACACHE_OK: return "ok";
+        case ACACHE_ERR_INVALID_ARG: return "invalid argument";
+        case ACACHE_ERR_UNSUPPORTED: return "unsupported dtype/head_dim";
+        case ACACHE_ERR_CUDA: return "CUDA launch error";
+        case ACACHE_ERR_WORKSPACE: return "workspace too small";
+        case ACACHE_ERR_TIMEOUT: return "bounded wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int acache_version(void) { return 100; }   // 0.1.0
+
+size_t acache_probe_workspace_bytes(const acache_attn_desc* a, int batch, int seq_len,
+                                    int affix_len, int num_masked) {
+    (void)num_masked;
+    if (!a || batch < 0 || affix_len < 0 || seq_len < affix_len || a->num_q_heads <= 0) return 0;
+    return carve_probe_ws(nullptr, batch, a->num_q_heads, seq_len - affix_len, affix_len).bytes;
+}
+
+int acache_probe_scores(const acache_attn_desc* desc, int batch, int seq_len, int affix_begin,
+                        int affix_len, const int32_t* masked_rows, int num_masked,
+                        const void* q, const void* k_req, const void* v_req,
+                        const void* k_affix, const void* v_affix, void* out, float* scores,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream_) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    const int T = seq_len, l = affix_begin, L = affix_len, m = num_masked;
+    if (batch < 0 || T < 0 || l < 0 || L < 0 || (int64_t)l + L > T || m < 0 || m > T - L)
+        return ACACHE_ERR_INVALID_ARG;
+    const int P = T - L;
+    if (batch == 0 || P == 0) return ACACHE_OK;      // no probe rows: nothing attends
+    if (!q || !k_req || !v_req || (L > 0 && (!k_affix || !v_affix)) || (m > 0 && !masked_rows) ||
+        (L > 0 && !scores))
+        return ACACHE_ERR_INVALID_ARG;
+    const ProbeWorkspace ws = carve_probe_ws(workspace, batch, a.hq, P, L);
+    if (!workspace || workspace_bytes < ws.bytes) return ACACHE_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k_req) || !aligned16(v_req) || !aligned16(k_affix) ||
+        !aligned16(v_affix) || !aligned16(out) || ((uintptr_t)workspace & 255u))
+        return ACACHE_ERR_INVALID_ARG;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    int rc;
+    if (tc_supported(a)) {
+        rc = launch_tc_probe_pass_a(a, batch, T, l, L, q, k_req, v_req, k_affix, v_affix, out,
+                                    ws.stat_m, ws.stat_l, dev_status, stream);
+    } else {
+        rc = launch_simt_probe_pass_a(a, batch, T, l, L, q, k_req, v_req, k_affix, v_affix, out,
+                                      ws.stat_m, ws.stat_l, stream);
+    }
+    if (rc) return rc;
+    if (L == 0) return ACACHE_OK;
+    if (tc_supported(a)) {
+        rc = launch_tc_probe_pass_b(a, batch, T, L, masked_rows, m, q, k_affix, ws.stat_m,
+                                    ws.stat_l, ws.partial, dev_status, stream);
+    } else {
+        rc = launch_simt_probe_pass_b(a, batch, T, L, masked_rows, m, q, k_affix, ws.stat_m,
+                                      ws.stat_l, ws.partial, dev_status, stream);
+    }
+    if (rc) return rc;
+    return launch_score_reduce(batch, a.hq, L, ws.partial, scores, stream);
+}
+
+int acache_topk_anchors(const float* scores, int batch, int affix_len, int k, int32_t* anchors,
+                        int32_t* dev_status, void* stream) {
+    if (batch < 0 || affix_len < 0 || k < 0 || k > affix_len) return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || k == 0) return ACACHE_OK;
+    if (!scores || !anchors) return ACACHE_ERR_INVALID_ARG;
+    return launch_topk(scores, batch, affix_len, k, anchors, dev_status, (cudaStream_t)stream);
+}
+
+int acache_build_slot_maps(int batch, int seq_len, int affix_begin, int affix_len, int k,
+                           const int32_t* anchors, const int32_t* shared_slot,
+                           const int32_t* private_slots, int32_t* write_pos, int32_t* read_slot,
+                           int32_t* dev_status, void* stream) {
+    const int T = seq_len, l = affix_begin, L = affix_len;
+    if (batch < 0 || T < 0 || l < 0 || L < 0 || (int64_t)l + L > T || k < 0 || k > L)
+        return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || T == 0) return ACACHE_OK;
+    const int R = k + T - L;
+    if ((k > 0 && !anchors) || (L > k && !shared_slot) || (R > 0 && (!private_slots || !write_pos)) ||
+        !read_slot)
+        return ACACHE_ERR_INVALID_ARG;
+    return launch_build_maps(batch, T, l, L, k, anchors, shared_slot, private_slots, write_pos,
+                             read_slot, dev_status, (cudaStream_t)stream);
+}
+
+int acache_write_slots(const acache_attn_desc* desc, int batch, int rows,
+                       const int32_t* write_slot, const void* k_new, const void* v_new,
+                       void* k_cache, void* v_cache, int64_t num_slots, int64_t private_begin,
+                       int32_t* dev_status, void* stream) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (batch < 0 || rows < 0 || num_slots < 0 || private_begin < 0 || private_begin > num_slots)
+        return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || rows == 0) return ACACHE_OK;
+    if (!write_slot || !k_new || !v_new || !k_cache || !v_cache) return ACACHE_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return ACACHE_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)a.hkv * a.d * elem_bytes(a.dtype);
+    return launch_write_slots(batch, rows, write_slot, k_new, v_new, k_cache, v_cache, row_bytes,
+                              num_slots, private_begin, dev_status, (cudaStream_t)stream);
+}
+
+int acache_slot_attention(const acache_attn_desc* desc, int batch, int n_q, const void* q,
+                          int seq_len, const int32_t* read_slot, const void* k_cache,
+                          const void* v_cache, int64_t num_slots, void* out,
+                          int32_t* dev_status, void* stream_) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (batch < 0 || n_q < 0 || seq_len < 0 || num_slots < 0) return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || n_q == 0) return ACACHE_OK;
+    if (seq_len == 0) return ACACHE_ERR_INVALID_ARG;       // a softmax over no keys
+    if (!q || !read_slot || !k_cache || !v_cache || !out) return ACACHE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return ACACHE_ERR_INVALID_ARG;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (tc_supported(a))
+        return launch_tc_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
+                                        num_slots, out, dev_status, stream);
+    return launch_simt_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
+                                      num_slots, out, dev_status, stream);
+}
+
+int acache_gather_slots(const acache_attn_desc* desc, int batch, int seq_len,
+                        const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                        int64_t num_slots, void* k_out, void* v_out, int32_t* dev_status,
+                        void* stream) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (batch < 0 || seq_len < 0 || num_slots < 0) return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || seq_len == 0) return ACACHE_OK;
+    if (!read_slot || !k_cache || !v_cache || !k_out || !v_out) return ACACHE_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_out) || !aligned16(v_out))
+        return ACACHE_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)a.hkv * a.d * elem_bytes(a.dtype);
+    return launch_gather_slots(batch, seq_len, read_slot, k_cache, v_cache, row_bytes, num_slots,
+                               k_out, v_out, dev_status, (cudaStream_t)stream);
+}
+
+}  // extern "C"

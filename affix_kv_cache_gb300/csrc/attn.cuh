@@ -1,0 +1,93 @@
+// attn.cuh -- key sources and launch declarations shared by the attention kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace acache {
+
+struct AttnArgs {
+    int hq, hkv, d, dtype;
+    float scale;
+};
+
+// Keys of the read-slot attention: logical key t of request b lives in physical slot
+// read_slot[b][t] of the layer's pool (Sec. 4.1, App. C.1).  An out-of-range slot reads
+// as a zero row and is flagged.
+template <typename T>
+struct SlotKeys {
+    const T* k_cache;
+    const T* v_cache;
+    const int32_t* read_slot;
+    int64_t num_slots;
+    int T_len;
+    int hkv;
+    int d;
+    ACACHE_DEVFN bool rows(int b, int t, int hk, const T*& kr, const T*& vr,
+                           int32_t* dev_status) const {
+        const int64_t s = read_slot[(int64_t)b * T_len + t];
+        if (s < 0 || s >= num_slots) {
+            flag(dev_status, ACACHE_DEV_BAD_SLOT);
+            return false;
+        }
+        const int64_t off = (s * hkv + hk) * d;
+        kr = k_cache + off;
+        vr = v_cache + off;
+        return true;
+    }
+};
+
+// Keys of the probe: logical key t is the shared affix row t - l for t in F = [l, l+L),
+// otherwise the request's own row (non-affix rows in ascending logical order) (Sec. 3.2).
+template <typename T>
+struct ProbeKeys {
+    const T* k_req;
+    const T* v_req;
+    const T* k_aff;
+    const T* v_aff;
+    int l, L, P, hkv, d;
+    ACACHE_DEVFN bool rows(int b, int t, int hk, const T*& kr, const T*& vr, int32_t*) const {
+        if (t >= l && t < l + L) {
+            const int64_t off = ((int64_t)(t - l) * hkv + hk) * d;
+            kr = k_aff + off;
+            vr = v_aff + off;
+        } else {
+            const int pr = t < l ? t : t - L;
+            const int64_t off = (((int64_t)b * P + pr) * hkv + hk) * d;
+            kr = k_req + off;
+            vr = v_req + off;
+        }
+        return true;
+    }
+};
+
+// ---- launchers (host) ---------------------------------------------------------------
+int launch_simt_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
+                               const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                               int64_t num_slots, void* out, int32_t* dev_status,
+                               cudaStream_t stream);
+int launch_simt_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
+                             const void* k_req, const void* v_req, const void* k_aff,
+                             const void* v_aff, void* out, float* stat_m, float* stat_l,
+                             cudaStream_t stream);
+int launch_simt_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int32_t* masked_rows,
+                             int m, const void* q, const void* k_aff, const float* stat_m,
+                             const float* stat_l, float* partial, int32_t* dev_status,
+                             cudaStream_t stream);
+int launch_score_reduce(int B, int Hq, int L, const float* partial, float* scores,
+                        cudaStream_t stream);
+
+int launch_write_slots(int batch, int rows, const int32_t* write_slot, const void* k_new,
+                       const void* v_new, void* k_cache, void* v_cache, int64_t row_bytes,
+                       int64_t num_slots, int64_t private_begin, int32_t* dev_status,
+                       cudaStream_t stream);
+int launch_gather_slots(int batch, int seq_len, const int32_t* read_slot, const void* k_cache,
+                        const void* v_cache, int64_t row_bytes, int64_t num_slots, void* k_out,
+                        void* v_out, int32_t* dev_status, cudaStream_t stream);
+int launch_build_maps(int batch, int T, int l, int L, int K, const int32_t* anchors,
+                      const int32_t* shared_slot, const int32_t* private_slots,
+                      int32_t* write_pos, int32_t* read_slot, int32_t* dev_status,
+                      cudaStream_t stream);
+int launch_topk(const float* scores, int batch, int L, int K, int32_t* anchors,
+                int32_t* dev_status, cudaStream_t stream);
+
+}  // namespace acache

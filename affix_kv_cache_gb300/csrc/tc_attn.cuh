@@ -1,0 +1,24 @@
+// tc_attn.cuh -- tensor-core (tcgen05 + TMEM) attention kernels for bf16, head_dim 128.
+#pragma once
+
+#include "attn.cuh"
+
+namespace acache {
+
+// True when the tcgen05 kernels cover this geometry (bf16, head_dim 128).
+bool tc_supported(const AttnArgs& a);
+
+int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
+                             const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                             int64_t num_slots, void* out, int32_t* dev_status,
+                             cudaStream_t stream);
+int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
+                           const void* k_req, const void* v_req, const void* k_aff,
+                           const void* v_aff, void* out, float* stat_m, float* stat_l,
+                           int32_t* dev_status, cudaStream_t stream);
+int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int32_t* masked_rows,
+                           int m, const void* q, const void* k_aff, const float* stat_m,
+                           const float* stat_l, float* partial, int32_t* dev_status,
+                           cudaStream_t stream);
+
+}  // namespace acache

@@ -1,0 +1,421 @@
+"""Benchmark of the affix-cache attention hot path on one GB300 (replicas for N > 1).
+
+One step = one pass of the whole path over one batch of the LLaDA-8B-shaped prefix
+workload (32 layers, 32 heads, head_dim 128, batch 4, affix L = 1024, 128 request +
+256 masked rows, anchor ratio 0.2 -> K = 205, R = 589, 8 recompute points):
+  anchor probe of all 32 layers (probe forward + masked-to-affix mass)  -> scores
+  Top-K anchors -> admission maps
+  8 recompute points x 32 layers x (anchor_write of R rows + slot attention R x T).
+
+Prints ONE JSON line (rank 0).  Metric: probe + slot-attention TFLOP/s (algorithmic
+flops: 4*P*T*d per probe row-head-layer, 4*R*T*d per recompute row-head-layer).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from affix_kv_cache_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "probe+slot_attn TFLOP/s & % of GB300 bf16 peak; anchor-scored tokens/s"
+DEFAULT_WORKLOAD = wl.LLADA_PREFIX.name
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.CATALOGUE))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle sample")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- flops
+def probe_flops(w, batch=None):
+    return 4.0 * w.P * w.T * w.d * w.hq * w.layers * (batch or w.batch)
+
+
+def slot_flops_per_launch(w, batch=None):
+    return 4.0 * w.R * w.T * w.d * w.hq * (batch or w.batch)
+
+
+def step_flops(w):
+    return probe_flops(w) + slot_flops_per_launch(w) * w.layers * w.recompute_points
+
+
+# ----------------------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def profiled_traffic(kernel_files):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
+    if the summary is missing or the kernel source changed since it was captured."""
+    import hashlib
+    summ = os.path.join(ROOT, "profiles", "slot_attention_llada8b_prefix.md")
+    if not os.path.exists(summ):
+        return None
+    fields = {}
+    for line in open(summ):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    h = hashlib.sha256()
+    for f in kernel_files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if fields.get("source_sha256") != h.hexdigest()[:16]:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, device_index=0):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9 or not parts[0].isdigit() or int(parts[0]) != device_index:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        under = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(under) if under else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- the path
+class Path:
+    """Device-resident inputs of one workload plus the sequence of C-ABI calls of a step."""
+
+    def __init__(self, w, device, seed_offset=0):
+        import affix_kv_cache_gb300 as ac
+        self.ac = ac
+        self.w = w = w.replace(seed=w.seed + seed_offset)
+        self.dev = device
+        self.desc = ac.attn_desc(w.hq, w.hkv, w.d, w.scale, w.dtype)
+        lay = wl.slot_layout(w, device)
+        self.lay = lay
+        self.masked = torch.tensor(w.masked_rows(), dtype=torch.int32, device=device).expand(
+            w.batch, -1).contiguous()
+        self.probe = [wl.probe_inputs(w, n, device) for n in range(w.layers)]
+        self.rec = [wl.recompute_inputs(w, n, 0, device) for n in range(w.layers)]
+        self.kc = [torch.zeros((lay.num_slots, w.hkv, w.d), dtype=w.torch_dtype, device=device)
+                   for _ in range(w.layers)]
+        self.vc = [torch.zeros_like(k) for k in self.kc]
+        for n in range(w.layers):   # register the shared affix cache once (admission)
+            ac.acache_write_slots(self.desc, 1, w.L, lay.shared_slot, self.probe[n]["k_aff"],
+                                  self.probe[n]["v_aff"], self.kc[n], self.vc[n], lay.num_slots, 0)
+        self.scores = torch.zeros((w.batch, w.L), dtype=torch.float32, device=device)
+        self.ws_bytes = ac.acache_probe_workspace_bytes(self.desc, w.batch, w.T, w.L, w.m)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.probe_out = torch.empty_like(self.probe[0]["q"])
+        self.anchors = torch.empty((w.batch, w.K), dtype=torch.int32, device=device)
+        self.write_pos = torch.empty((w.batch, w.R), dtype=torch.int32, device=device)
+        self.read_slot = torch.empty((w.batch, w.T), dtype=torch.int32, device=device)
+        self.out = [torch.empty_like(r["q_r"]) for r in self.rec]
+        self.launches_per_step = w.layers * 3 + 2 + w.recompute_points * w.layers * 2
+        torch.cuda.synchronize()
+
+    def step(self, ev=None):
+        """One pass of the path.  `ev` (optional) collects CUDA events around phases."""
+        ac, w, lay = self.ac, self.w, self.lay
+        s = torch.cuda.current_stream()
+        self.scores.zero_()
+        if ev is not None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+        for n in range(w.layers):
+            p = self.probe[n]
+            ac.acache_probe_scores(self.desc, w.batch, w.T, w.l, w.L, self.masked, w.m, p["q"],
+                                   p["k_req"], p["v_req"], p["k_aff"], p["v_aff"], self.probe_out,
+                                   self.scores, self.ws, self.ws_bytes)
+        ac.acache_topk_anchors(self.scores, w.batch, w.L, w.K, self.anchors)
+        if ev is not None:
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(s)
+            ev["select"].append((e0, e1))
+        ac.acache_build_slot_maps(w.batch, w.T, w.l, w.L, w.K, self.anchors, lay.shared_slot,
+                                  lay.private_slots, self.write_pos, self.read_slot)
+        for _ in range(w.recompute_points):
+            for n in range(w.layers):
+                r = self.rec[n]
+                ac.acache_write_slots(self.desc, w.batch, w.R, lay.private_slots, r["k_new"],
+                                      r["v_new"], self.kc[n], self.vc[n], lay.num_slots,
+                                      lay.private_begin)
+                if ev is not None:
+                    a = torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                ac.acache_slot_attention(self.desc, w.batch, w.R, r["q_r"], w.T, self.read_slot,
+                                         self.kc[n], self.vc[n], lay.num_slots, self.out[n])
+                if ev is not None:
+                    b = torch.cuda.Event(enable_timing=True)
+                    b.record(s)
+                    ev["slot"].append((a, b))
+
+    # ---- host buffers for the end-to-end measurement ---------------------------------
+    def host_inputs(self):
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        self.h_probe = [{k: pin(v) for k, v in p.items() if k in ("q", "k_req", "v_req")}
+                        for p in self.probe]
+        self.h_rec = [{k: pin(v) for k, v in r.items()} for r in self.rec]
+        self.h_anchors = torch.empty(self.anchors.shape, dtype=torch.int32).pin_memory()
+        self.h_scores = torch.empty(self.scores.shape, dtype=torch.float32).pin_memory()
+        self.h_out = torch.empty(self.out[-1].shape, dtype=self.out[-1].dtype).pin_memory()
+        bi = sum(t.numel() * t.element_size() for p in self.h_probe for t in p.values())
+        bi += sum(t.numel() * t.element_size() for r in self.h_rec for t in r.values())
+        bo = sum(t.numel() * t.element_size() for t in (self.h_anchors, self.h_scores, self.h_out))
+        return bi, bo
+
+    def step_e2e(self):
+        for n in range(self.w.layers):
+            for k, v in self.h_probe[n].items():
+                self.probe[n][k].copy_(v, non_blocking=True)
+            for k, v in self.h_rec[n].items():
+                self.rec[n][k].copy_(v, non_blocking=True)
+        self.step()
+        self.h_anchors.copy_(self.anchors, non_blocking=True)
+        self.h_scores.copy_(self.scores, non_blocking=True)
+        self.h_out.copy_(self.out[-1], non_blocking=True)
+
+
+# ----------------------------------------------------------------------------- oracle
+def cpu_oracle_sample(w, budget_s):
+    """Time the oracle as it stands on a bounded sample of the workload: request 0, layer by
+    layer, the probe of all heads and then the slot attention of a slice of the recomputed
+    rows, until the budget is spent.  Returns (flops, seconds, cores, description)."""
+    import numpy as np
+    import oracle
+    w1 = w.replace(batch=1)
+    lay = wl.slot_layout(w1)
+    flops, t_total, done = 0.0, 0.0, []
+    cores = oracle.get_threads()
+    masked = w.masked_rows()
+    rows_per_call = 64
+    n = 0
+    while t_total < budget_s and n < w.layers:
+        p = wl.probe_inputs(w1, n)
+        t0 = time.perf_counter()
+        oracle.probe_layer(p["q"], p["k_req"], p["v_req"], p["k_aff"], p["v_aff"], T=w.T, l=w.l,
+                           masked_rows=masked, scale=w.scale)
+        t_total += time.perf_counter() - t0
+        flops += probe_flops(w1) / w.layers
+        done.append(f"probe L{n}")
+        if t_total >= budget_s:
+            break
+        r = wl.recompute_inputs(w1, n)
+        rs = np.empty((1, w.T), np.int32)
+        anchors = np.arange(w.K, dtype=np.int32)[None]
+        _, rs = oracle.build_slot_maps(anchors, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+        kc = torch.zeros((lay.num_slots, w.hkv, w.d), dtype=w.torch_dtype)
+        kc[lay.private_slots[0].long()] = r["k_new"][0]
+        kc[lay.shared_slot.long()] = p["k_aff"]
+        vc = torch.zeros_like(kc)
+        vc[lay.private_slots[0].long()] = r["v_new"][0]
+        vc[lay.shared_slot.long()] = p["v_aff"]
+        rows = list(range(min(rows_per_call, w.R)))
+        t0 = time.perf_counter()
+        oracle.slot_attention(r["q_r"], rs, kc, vc, scale=w.scale, rows=rows)
+        t_total += time.perf_counter() - t0
+        flops += 4.0 * len(rows) * w.T * w.d * w.hq
+        done.append(f"slot L{n} rows 0..{len(rows) - 1}")
+        n += 1
+    desc = (f"oracle (float64 C, OpenMP {cores} threads) on request 0: {', '.join(done[:4])}"
+            f"{' ...' if len(done) > 4 else ''} ({len(done)} calls, {t_total:.1f} s)")
+    return flops, t_total, cores, desc
+
+
+# ----------------------------------------------------------------------------- main
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    flops, secs, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
+    v = flops / secs / 1e12
+    per_step_s = secs
+    line = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, shapes of the LLaDA-8B prefix workload)",
+            "config": {"workload": w.name, **{k: v2 for k, v2 in w.describe().items() if k != "workload"}},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = wl.CATALOGUE[args.workload]
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    path = Path(w, dev, seed_offset=rank)
+    for _ in range(max(args.warmup, 3)):
+        path.step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([x], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+    ev = {"select": [], "slot": []}
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/acache_clocks_{rank}.csv")
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with clocks:
+        start.record()
+        for _ in range(args.steps):
+            path.step(ev)
+        end.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(start.elapsed_time(end))
+    ms_per_step = ms / args.steps
+    tflops = step_flops(w) * args.steps * world / (ms / 1e3) / 1e12
+    slot_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["slot"])
+    select_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["select"])
+    scored_tok_s = w.batch * w.L / (select_ms / 1e3)
+    peaks = measured_peaks()
+    slot_achieved = slot_flops_per_launch(w) / (slot_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = profiled_traffic(["affix_kv_cache_gb300/csrc/tc_attn.cu"])
+
+    e2e = None
+    if not args.no_e2e:
+        bi, bo = path.host_inputs()
+        path.step_e2e()
+        torch.cuda.synchronize()
+        barrier()
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_s.record()
+        n_e2e = max(1, min(args.steps, 5))
+        for _ in range(n_e2e):
+            path.step_e2e()
+        e_e.record()
+        torch.cuda.synchronize()
+        barrier()
+        ems = max_over_ranks(e_s.elapsed_time(e_e))
+        e2e = {"value": step_flops(w) * n_e2e * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "ms_per_step": ems / n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        flops, secs, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        gb_touched = sum(t.numel() * t.element_size() for p in path.probe for t in p.values()) + \
+            sum(t.numel() * t.element_size() for r in path.rec for t in r.values()) + \
+            2 * sum(k.numel() * k.element_size() for k in path.kc)
+        line = {
+            "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; LLaDA-8B attention shapes, no weights or datasets)",
+            "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": f"inputs larger than L2: {gb_touched / 1e9:.1f} GB touched per step"},
+            "anchor_scored_tokens_per_s": scored_tok_s,
+            "select_ms": select_ms,
+            "slot_attn_ms_per_launch": slot_ms,
+            "roofline": {"bound": "tensor", "kernel": "slot_attention", "achieved": slot_achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": slot_achieved / peak,
+                         "peak_source": f"{peaks['source']} bf16 sustained", "traffic": traffic},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": path.launches_per_step * args.steps,
+            "clocks": clocks.summary(local),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/*
+ * acache.h -- C ABI of libacache.so, the GB300 (sm_103a) affix-cache attention path.
+ *
+ * The path follows the page "Affix Cache for Diffusion Large Language Models"
+ * (arXiv 2608.26140):
+ *   (1) anchor probe: the request's non-affix rows attend once over the shared
+ *       precomputed affix K/V plus the request's own K/V (Sec. 3.2);
+ *   (2) importance s_j: masked-to-affix attention mass summed over layers, heads and the
+ *       initially masked rows (Sec. 3.2, Eq. 4-5);
+ *   (3) anchors A = TopK({s_j}, K) (Sec. 3.2, Eq. 6);
+ *   (4) store-then-attend: fresh anchor and request K/V are written to private slots and
+ *       attention reads every logical position through a per-request read-slot map
+ *       (Sec. 4.1, 4.3; App. C.1).
+ *
+ * Conventions for every call
+ * --------------------------
+ *  - Pointers are DEVICE pointers unless a comment says otherwise; the caller owns all
+ *    memory.  The library never allocates device memory and creates no stream or event.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
+ *    legacy default stream) and returns an acache_status synchronously.
+ *  - Synchronous errors: ACACHE_ERR_INVALID_ARG (a required pointer is NULL or a scalar
+ *    is out of range; nothing is launched), ACACHE_ERR_UNSUPPORTED (dtype / head_dim
+ *    combination not built), ACACHE_ERR_CUDA (a launch failed; the CUDA error is cleared).
+ *  - Asynchronous data errors: an index that would address memory outside its buffer is
+ *    skipped (no access) and, when `dev_status` is non-NULL, the matching ACACHE_DEV_*
+ *    bit is OR-ed into *dev_status.  Bounded waits that give up set ACACHE_DEV_TIMEOUT.
+ *  - Layouts are row-major and contiguous: Q/O and fresh K/V are token-major
+ *    [batch][rows][heads][head_dim]; a layer's KV pool is [num_slots][Hkv][head_dim]
+ *    (K and V in separate pools, the caller passes each layer's base pointers).
+ *  - Symbols: B batch, T logical length, F = [l, l+L) the affix span, P = T - L probe rows
+ *    (non-affix positions in ascending logical order), m initially masked rows,
+ *    K anchor budget, R = K + P recomputed rows, Hq / Hkv query / KV heads, d head dim.
+ */
+#ifndef ACACHE_H_
+#define ACACHE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ACACHE_API __attribute__((visibility("default")))
+#else
+#define ACACHE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ACACHE_OK = 0,
+    ACACHE_ERR_INVALID_ARG = -1,
+    ACACHE_ERR_UNSUPPORTED = -2,
+    ACACHE_ERR_CUDA = -3,
+    ACACHE_ERR_WORKSPACE = -4,
+    ACACHE_ERR_TIMEOUT = -5
+} acache_status;
+
+typedef enum { ACACHE_F32 = 0, ACACHE_BF16 = 1 } acache_dtype;
+
+/* bits OR-ed into *dev_status by kernels */
+enum {
+    ACACHE_DEV_BAD_SLOT = 1,      /* a slot index outside [0, num_slots)                  */
+    ACACHE_DEV_SHARED_WRITE = 2,  /* a write slot below private_begin (shared region)     */
+    ACACHE_DEV_BAD_ROW = 4,       /* a masked-row index outside [0, P)                     */
+    ACACHE_DEV_BAD_ANCHOR = 8,    /* anchors not strictly ascending offsets in [0, L)      */
+    ACACHE_DEV_NAN = 16,          /* a NaN importance score reached Top-K                  */
+    ACACHE_DEV_TIMEOUT = 32       /* a bounded wait inside a kernel gave up                */
+};
+
+/* Attention geometry shared by the attention calls. */
+typedef struct {
+    int32_t num_q_heads;    /* Hq                                                    */
+    int32_t num_kv_heads;   /* Hkv, Hq % Hkv == 0; query head h reads KV head h/(Hq/Hkv) */
+    int32_t head_dim;       /* d: 64 or 128                                          */
+    float scale;            /* softmax scale, normally 1/sqrt(d) (Eq. 4)             */
+    int32_t dtype;          /* acache_dtype of Q, K, V and O                         */
+} acache_attn_desc;
+
+/* Human-readable name of a status code (host, static storage). */
+ACACHE_API const char* acache_status_string(int status);
+/* Library version: major*10000 + minor*100 + patch. */
+ACACHE_API int acache_version(void);
+
+/* ---------------------------------------------------------------------------------
+ * (1)+(2) Anchor probe of ONE layer and its importance contribution.
+ * Page: Sec. 3.2, Eq. 4-5 ("one-shot probe over the current request's non-affix
+ * positions while using the precomputed affix cache as fixed past KV states").
+ *
+ * For each request b, query head h and probe row k (P rows), the row attends over all T
+ * logical keys: K_log[t] = k_affix[t-l] for t in F, else the request's own k_req row
+ * (value rows likewise).  Softmax runs over the full row.  Then, for every initially
+ * masked row k and affix offset j:  scores[b][j] += softmax_row_k[l + j], summed over
+ * heads in ascending order.  Call layers 0..N-1 in order on one stream, after zeroing
+ * `scores`; that fixes the accumulation order, so results are bit-reproducible.
+ *
+ *   q            [B][P][Hq][d]   probe-row queries, rows in ascending logical order
+ *   k_req, v_req [B][P][Hkv][d]  the request's own K/V rows (same order)
+ *   k_affix, v_affix [L][Hkv][d] shared precomputed affix cache (one copy for all b)
+ *   masked_rows  [B][m] int32    indices into the P probe rows; bad ones are skipped
+ *                                and flagged ACACHE_DEV_BAD_ROW
+ *   out          [B][P][Hq][d]   attention output of the probe rows, or NULL
+ *   scores       [B][L] float    importance, ACCUMULATED in place
+ *   workspace    >= acache_probe_workspace_bytes(...) bytes, 256-byte aligned; its
+ *                contents need no initialisation and are clobbered
+ * Returns ACACHE_ERR_WORKSPACE if the workspace is too small.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API size_t acache_probe_workspace_bytes(const acache_attn_desc* a, int batch, int seq_len,
+                                    int affix_len, int num_masked);
+ACACHE_API int acache_probe_scores(const acache_attn_desc* a, int batch, int seq_len, int affix_begin,
+                        int affix_len, const int32_t* masked_rows, int num_masked,
+                        const void* q, const void* k_req, const void* v_req,
+                        const void* k_affix, const void* v_affix, void* out, float* scores,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * (3) Anchor selection.  Page: Sec. 3.2, Eq. 6, A = TopK({s_j}, K), S = F \ A.
+ * anchors[b] receives the K affix offsets with the largest scores, ties broken toward the
+ * lower offset, written in ascending offset order.  -0.0 counts as +0.0.  A NaN score
+ * flags ACACHE_DEV_NAN (NaN ranks below every number).  0 <= K <= L.
+ *   scores  [B][L] float, anchors [B][K] int32
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_topk_anchors(const float* scores, int batch, int affix_len, int k,
+                        int32_t* anchors, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Admission-time maps.  Page: Sec. 4.1-4.2 (write-side recomputation map and per-request
+ * read-slot map, recorded once at admission).
+ * The R = K + P recomputed logical positions are the anchor positions l + A_b and every
+ * non-affix position, in ascending order.
+ *   write_pos[b][i] = the i-th recomputed logical position            [B][R] int32
+ *   read_slot[b][t] = private_slots[b][i] if t is the i-th recomputed position,
+ *                     shared_slot[t - l] otherwise (non-anchor affix)  [B][T] int32
+ * The write-side slot of row i is private_slots[b][i] itself.
+ *   anchors [B][K] (strictly ascending offsets in [0, L); otherwise that request's maps
+ *   are left untouched and ACACHE_DEV_BAD_ANCHOR is flagged), shared_slot [L],
+ *   private_slots [B][R].
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_build_slot_maps(int batch, int seq_len, int affix_begin, int affix_len, int k,
+                           const int32_t* anchors, const int32_t* shared_slot,
+                           const int32_t* private_slots, int32_t* write_pos,
+                           int32_t* read_slot, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * (4a) Store step of one layer.  Page: Sec. 4.3 and App. C.1 (store-then-attend through
+ * the write-side slot mapping).
+ *   k_cache[write_slot[b][i]] = k_new[b][i] (all KV heads), same for V.
+ * A slot outside [0, num_slots) is skipped (ACACHE_DEV_BAD_SLOT); a slot below
+ * private_begin is skipped (ACACHE_DEV_SHARED_WRITE), which protects the shared region.
+ * Pass private_begin = 0 to register a shared affix itself.
+ *   write_slot [B][R] int32, k_new / v_new [B][R][Hkv][d], caches [num_slots][Hkv][d]
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_write_slots(const acache_attn_desc* a, int batch, int rows,
+                       const int32_t* write_slot, const void* k_new, const void* v_new,
+                       void* k_cache, void* v_cache, int64_t num_slots,
+                       int64_t private_begin, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * (4b) Read-slot attention of one layer.  Page: Sec. 4.3 (queries only for recomputed
+ * positions, keys and values read through the read-slot map) and App. C.1.
+ * Each of the n_q dense query rows of request b attends bidirectionally over all T
+ * logical keys K_log[t] = k_cache[read_slot[b][t]] (V likewise).
+ *   q [B][n_q][Hq][d], read_slot [B][T] int32, caches [num_slots][Hkv][d],
+ *   out [B][n_q][Hq][d].  A slot outside [0, num_slots) reads as a zero key and value
+ *   row (no access) and flags ACACHE_DEV_BAD_SLOT.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_slot_attention(const acache_attn_desc* a, int batch, int n_q, const void* q,
+                          int seq_len, const int32_t* read_slot, const void* k_cache,
+                          const void* v_cache, int64_t num_slots, void* out,
+                          int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Logical KV view.  Page: Sec. 4.1 ("the same logical full-context KV view").
+ * Materialises k_out[b][t] = k_cache[read_slot[b][t]] (V likewise), [B][T][Hkv][d].
+ * Bad slots are skipped (the output row is left untouched) and flag ACACHE_DEV_BAD_SLOT.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_gather_slots(const acache_attn_desc* a, int batch, int seq_len,
+                        const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                        int64_t num_slots, void* k_out, void* v_out, int32_t* dev_status,
+                        void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ACACHE_H_ */

@@ -1,0 +1,305 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle on the same seeded inputs.
+
+Sizes are small enough for the oracle to finish in seconds but span several 128-row /
+128-key tiles with ragged tails.  Tolerances are those of the path (see gpu_helpers).
+"""
+import numpy as np
+import pytest
+import torch
+
+import affix_kv_cache_gb300 as ac
+import oracle
+from affix_kv_cache_gb300 import workloads as wl
+
+from gpu_helpers import (assert_anchors_match, assert_out_close, assert_scores_close, desc_of, dev,
+                         probe_layer_gpu, register_shared, status_tensor)
+
+pytestmark = pytest.mark.gpu
+
+
+def tiny(segments, hq=4, hkv=2, d=128, batch=2, ratio=200, dtype="bf16", **kw):
+    return wl.Workload(name="parity", dtype=dtype, layers=1, hq=hq, hkv=hkv, d=d, batch=batch,
+                       segments=tuple(segments), ratio_permille=ratio, recompute_points=1, **kw)
+
+
+# several tiles with ragged tails: P = 300 probe rows, m = 150 masked, L = 400, T = 700
+RAGGED = {
+    "prefix": [(wl.SEG_AFFIX, 400), (wl.SEG_REQ, 150), (wl.SEG_MASK, 150)],
+    "infix": [(wl.SEG_REQ, 100), (wl.SEG_AFFIX, 400), (wl.SEG_REQ, 50), (wl.SEG_MASK, 150)],
+    "suffix": [(wl.SEG_REQ, 150), (wl.SEG_MASK, 150), (wl.SEG_AFFIX, 400)],
+}
+SMALL = [(wl.SEG_REQ, 5), (wl.SEG_AFFIX, 37), (wl.SEG_REQ, 3), (wl.SEG_MASK, 19)]
+
+
+# ------------------------------------------------------------------ store / gather / maps
+@pytest.mark.parametrize("dtype,d,heads", [("bf16", 128, (4, 2)), ("f32", 64, (2, 2)),
+                                           ("bf16", 64, (8, 8))])
+def test_write_slots_bit_exact(dtype, d, heads):
+    w = tiny(RAGGED["infix"], hq=heads[0], hkv=heads[1], d=d, dtype=dtype, batch=3, page=64)
+    lay = wl.slot_layout(w)
+    rec = wl.recompute_inputs(w, 0)
+    g = torch.Generator().manual_seed(3)
+    kc = torch.randn((lay.num_slots, w.hkv, w.d), generator=g).to(w.torch_dtype)
+    vc = torch.randn((lay.num_slots, w.hkv, w.d), generator=g).to(w.torch_dtype)
+    kb, vb, flags = oracle.write_slots(lay.private_slots, rec["k_new"], rec["v_new"], kc, vc,
+                                       private_begin=lay.private_begin)
+    kd, vd = dev(kc), dev(vc)
+    st = status_tensor()
+    ac.acache_write_slots(desc_of(w), w.batch, w.R, dev(lay.private_slots), dev(rec["k_new"]),
+                          dev(rec["v_new"]), kd, vd, lay.num_slots, lay.private_begin, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0 and flags == 0
+    assert np.array_equal(kd.cpu().view(torch.uint8).reshape(-1).numpy(), kb)
+    assert np.array_equal(vd.cpu().view(torch.uint8).reshape(-1).numpy(), vb)
+
+
+def test_write_slots_skips_and_flags_bad_slots():
+    w = tiny(SMALL, batch=2, page=16)
+    lay = wl.slot_layout(w)
+    rec = wl.recompute_inputs(w, 0)
+    ws = lay.private_slots.clone()
+    ws[0, 0] = 1                         # inside the shared region
+    ws[1, 3] = lay.num_slots + 5         # outside the pool
+    ws[1, 4] = -2
+    kc = torch.zeros((lay.num_slots, w.hkv, w.d), dtype=w.torch_dtype)
+    kb, vb, flags = oracle.write_slots(ws, rec["k_new"], rec["v_new"], kc, kc,
+                                       private_begin=lay.private_begin)
+    kd, vd = dev(kc), dev(kc.clone())
+    st = status_tensor()
+    ac.acache_write_slots(desc_of(w), w.batch, w.R, dev(ws), dev(rec["k_new"]), dev(rec["v_new"]),
+                          kd, vd, lay.num_slots, lay.private_begin, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == (ac._lib.DEV_BAD_SLOT | ac._lib.DEV_SHARED_WRITE) == flags
+    assert np.array_equal(kd.cpu().view(torch.uint8).reshape(-1).numpy(), kb)
+    assert np.array_equal(vd.cpu().view(torch.uint8).reshape(-1).numpy(), vb)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_gather_slots_bit_exact(dtype, d):
+    w = tiny(RAGGED["prefix"], d=d, dtype=dtype, batch=3, page=64)
+    lay = wl.slot_layout(w)
+    g = torch.Generator().manual_seed(5)
+    kc = torch.randn((lay.num_slots, w.hkv, w.d), generator=g).to(w.torch_dtype)
+    vc = torch.randn((lay.num_slots, w.hkv, w.d), generator=g).to(w.torch_dtype)
+    rs = torch.randint(0, lay.num_slots, (w.batch, w.T), generator=g, dtype=torch.int32)
+    ko, vo, flags = oracle.gather_slots(rs, kc, vc)
+    kd = torch.empty((w.batch, w.T, w.hkv, w.d), dtype=w.torch_dtype, device="cuda")
+    vd = torch.empty_like(kd)
+    ac.acache_gather_slots(desc_of(w), w.batch, w.T, dev(rs), dev(kc), dev(vc), lay.num_slots, kd, vd)
+    torch.cuda.synchronize()
+    assert np.array_equal(kd.cpu().view(torch.uint8).reshape(-1).numpy(), ko)
+    assert np.array_equal(vd.cpu().view(torch.uint8).reshape(-1).numpy(), vo)
+
+
+@pytest.mark.parametrize("layout", list(RAGGED))
+@pytest.mark.parametrize("ratio", [0, 200, 1000])
+def test_build_slot_maps_bit_exact(layout, ratio):
+    w = tiny(RAGGED[layout], ratio=ratio, batch=3, page=64)
+    lay = wl.slot_layout(w)
+    rng = np.random.default_rng(ratio + len(layout))
+    anchors = np.stack([np.sort(rng.choice(w.L, w.K, replace=False))
+                        for _ in range(w.batch)]).astype(np.int32).reshape(w.batch, w.K)
+    wp, rs = oracle.build_slot_maps(anchors, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+    wpd = torch.full((w.batch, w.R), -7, dtype=torch.int32, device="cuda")
+    rsd = torch.full((w.batch, w.T), -7, dtype=torch.int32, device="cuda")
+    st = status_tensor()
+    ac.acache_build_slot_maps(w.batch, w.T, w.l, w.L, w.K, dev(torch.from_numpy(anchors)),
+                              dev(lay.shared_slot), dev(lay.private_slots), wpd, rsd, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(wpd.cpu().numpy(), wp)
+    assert np.array_equal(rsd.cpu().numpy(), rs)
+
+
+def test_build_slot_maps_flags_bad_anchors():
+    w = tiny(SMALL, ratio=500, batch=2)
+    lay = wl.slot_layout(w)
+    anchors = torch.stack([torch.arange(w.K, dtype=torch.int32)] * 2)
+    anchors[1, 2] = anchors[1, 1]                    # not strictly ascending
+    rsd = torch.full((w.batch, w.T), -7, dtype=torch.int32, device="cuda")
+    wpd = torch.full((w.batch, w.R), -7, dtype=torch.int32, device="cuda")
+    st = status_tensor()
+    ac.acache_build_slot_maps(w.batch, w.T, w.l, w.L, w.K, dev(anchors), dev(lay.shared_slot),
+                              dev(lay.private_slots), wpd, rsd, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == ac._lib.DEV_BAD_ANCHOR
+    assert (rsd[1] == -7).all() and (rsd[0] != -7).all()     # request 1 untouched
+
+
+# ------------------------------------------------------------------ Top-K
+@pytest.mark.parametrize("L,K", [(1, 1), (37, 0), (37, 8), (400, 80), (1024, 205), (8192, 1639),
+                                 (3000, 3000), (50000, 777)])
+def test_topk_bit_exact(L, K):
+    g = torch.Generator().manual_seed(L + K)
+    s = torch.rand((4, L), generator=g)
+    s[1] = torch.round(s[1] * 8) / 8                 # heavy exact ties
+    s[2] = 0.5                                        # all equal
+    s[3, ::3] = 0.0
+    s[3, 1::3] = -0.0                                 # -0.0 ranks as +0.0
+    sd = dev(s)
+    a = torch.empty((4, K), dtype=torch.int32, device="cuda")
+    st = status_tensor()
+    ac.acache_topk_anchors(sd, 4, L, K, a, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    # the oracle decides on the very same float32 values (exact in float64)
+    want = oracle.topk_anchors(s.double().numpy(), K)
+    assert np.array_equal(a.cpu().numpy(), want)
+
+
+def test_topk_flags_nan():
+    s = torch.rand((1, 100))
+    s[0, 7] = float("nan")
+    a = torch.empty((1, 10), dtype=torch.int32, device="cuda")
+    st = status_tensor()
+    ac.acache_topk_anchors(dev(s), 1, 100, 10, a, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == ac._lib.DEV_NAN
+    assert 7 not in a.cpu().numpy()[0].tolist()
+
+
+# ------------------------------------------------------------------ probe
+@pytest.mark.parametrize("layout", list(RAGGED))
+@pytest.mark.parametrize("dtype,d,heads", [("bf16", 128, (4, 2)), ("f32", 64, (2, 2)),
+                                           ("bf16", 128, (7, 1))])
+def test_probe_parity(layout, dtype, d, heads):
+    w = tiny(RAGGED[layout], hq=heads[0], hkv=heads[1], d=d, dtype=dtype, batch=2)
+    inp = wl.probe_inputs(w, 0)
+    ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
+                             T=w.T, l=w.l, masked_rows=w.masked_rows(), scale=w.scale)
+    scores = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    o = probe_layer_gpu(w, inp, scores)
+    torch.cuda.synchronize()
+    assert_out_close(o.float().cpu().numpy(), ref["out"], dtype, "probe output")
+    assert_scores_close(scores.cpu().numpy(), ref["scores"], "probe scores")
+
+
+def test_probe_accumulates_over_layers_and_is_deterministic():
+    w = tiny(RAGGED["infix"], batch=2).replace(layers=3)
+    ref = None
+    s1 = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    s2 = torch.zeros_like(s1)
+    for n in range(w.layers):
+        inp = wl.probe_inputs(w, n)
+        ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
+                                 T=w.T, l=w.l, masked_rows=w.masked_rows(), scale=w.scale,
+                                 scores=None if ref is None else ref["scores"], want_out=False)
+        o1 = probe_layer_gpu(w, inp, s1)
+        o2 = probe_layer_gpu(w, inp, s2)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2)
+    assert torch.equal(s1, s2)
+    assert_scores_close(s1.cpu().numpy(), ref["scores"], "3-layer scores")
+
+
+def test_probe_bad_masked_row_is_skipped_and_flagged():
+    w = tiny(SMALL, batch=2, d=64, dtype="f32")
+    inp = wl.probe_inputs(w, 0)
+    masked = torch.tensor(w.masked_rows(), dtype=torch.int32).expand(w.batch, -1).clone()
+    masked[1, 0] = w.P + 3
+    ok_rows = masked[1, 1:].tolist()
+    ref0 = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
+                              T=w.T, l=w.l, masked_rows=w.masked_rows(), scale=w.scale, want_out=False)
+    ref1 = oracle.probe_layer(inp["q"][1:], inp["k_req"][1:], inp["v_req"][1:], inp["k_aff"],
+                              inp["v_aff"], T=w.T, l=w.l, masked_rows=ok_rows, scale=w.scale,
+                              want_out=False)
+    scores = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    st = status_tensor()
+    probe_layer_gpu(w, inp, scores, masked=masked, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == ac._lib.DEV_BAD_ROW
+    assert_scores_close(scores[0].cpu().numpy()[None], ref0["scores"][:1], "request 0")
+    assert_scores_close(scores[1].cpu().numpy()[None], ref1["scores"], "request 1")
+
+
+# ------------------------------------------------------------------ slot attention
+@pytest.mark.parametrize("dtype,d,heads", [("bf16", 128, (4, 2)), ("f32", 64, (2, 2)),
+                                           ("bf16", 128, (7, 1)), ("bf16", 64, (2, 1))])
+@pytest.mark.parametrize("n_q,T", [(300, 700), (1, 129), (129, 1)])
+def test_slot_attention_parity(dtype, d, heads, n_q, T):
+    hq, hkv = heads
+    g = torch.Generator().manual_seed(n_q * 7 + T)
+    B, num_slots = 2, 1500
+    td = torch.float32 if dtype == "f32" else torch.bfloat16
+    kc = torch.randn((num_slots, hkv, d), generator=g).to(td)
+    vc = torch.randn((num_slots, hkv, d), generator=g).to(td)
+    q = torch.randn((B, n_q, hq, d), generator=g).to(td)
+    rs = torch.randint(0, num_slots, (B, T), generator=g, dtype=torch.int32)
+    scale = d ** -0.5
+    ref = oracle.slot_attention(q, rs, kc, vc, scale=scale)
+    out = torch.empty((B, n_q, hq, d), dtype=td, device="cuda")
+    st = status_tensor()
+    ac.acache_slot_attention(ac.attn_desc(hq, hkv, d, scale, dtype), B, n_q, dev(q), T, dev(rs),
+                             dev(kc), dev(vc), num_slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(out.float().cpu().numpy(), ref, dtype, "slot attention")
+
+
+def test_slot_attention_bad_slot_reads_zero_row():
+    B, n_q, T, hq, hkv, d, num_slots = 1, 40, 150, 2, 2, 128, 300
+    g = torch.Generator().manual_seed(11)
+    kc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    q = torch.randn((B, n_q, hq, d), generator=g).to(torch.bfloat16)
+    rs = torch.randint(0, num_slots, (B, T), generator=g, dtype=torch.int32)
+    rs[0, 17] = num_slots + 100
+    # the oracle sees an extra all-zero slot in place of the bad one
+    kz = torch.cat([kc, torch.zeros(1, hkv, d, dtype=kc.dtype)])
+    vz = torch.cat([vc, torch.zeros(1, hkv, d, dtype=vc.dtype)])
+    rz = rs.clone()
+    rz[0, 17] = num_slots
+    ref = oracle.slot_attention(q, rz, kz, vz, scale=d ** -0.5)
+    out = torch.empty((B, n_q, hq, d), dtype=torch.bfloat16, device="cuda")
+    st = status_tensor()
+    ac.acache_slot_attention(ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16"), B, n_q, dev(q), T,
+                             dev(rs), dev(kc), dev(vc), num_slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == ac._lib.DEV_BAD_SLOT
+    assert_out_close(out.float().cpu().numpy(), ref, "bf16", "bad-slot attention")
+
+
+# ------------------------------------------------------------------ the tiny workload end to end
+def test_tiny_prefix_f32_pipeline():
+    """Probe -> scores -> Top-K(26) -> maps -> write 122 rows -> slot attention (122 x 224)."""
+    w = wl.TINY_PREFIX_F32
+    lay = wl.slot_layout(w)
+    inp = wl.probe_inputs(w, 0)
+    ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
+                             T=w.T, l=w.l, masked_rows=w.masked_rows(), scale=w.scale)
+    scores = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    o = probe_layer_gpu(w, inp, scores)
+    anchors = torch.empty((w.batch, w.K), dtype=torch.int32, device="cuda")
+    ac.acache_topk_anchors(scores, w.batch, w.L, w.K, anchors)
+    wp = torch.empty((w.batch, w.R), dtype=torch.int32, device="cuda")
+    rs = torch.empty((w.batch, w.T), dtype=torch.int32, device="cuda")
+    ac.acache_build_slot_maps(w.batch, w.T, w.l, w.L, w.K, anchors, dev(lay.shared_slot),
+                              dev(lay.private_slots), wp, rs)
+    kc = torch.zeros((lay.num_slots, w.hkv, w.d), dtype=torch.float32, device="cuda")
+    vc = torch.zeros_like(kc)
+    register_shared(w, lay, inp["k_aff"], inp["v_aff"], kc, vc)
+    rec = wl.recompute_inputs(w, 0)
+    ac.acache_write_slots(desc_of(w), w.batch, w.R, dev(lay.private_slots), dev(rec["k_new"]),
+                          dev(rec["v_new"]), kc, vc, lay.num_slots, lay.private_begin)
+    out = torch.empty((w.batch, w.R, w.hq, w.d), dtype=torch.float32, device="cuda")
+    ac.acache_slot_attention(desc_of(w), w.batch, w.R, dev(rec["q_r"]), w.T, rs, kc, vc,
+                             lay.num_slots, out)
+    torch.cuda.synchronize()
+    # step by step against the oracle
+    assert_out_close(o.cpu().numpy(), ref["out"], "f32", "probe output")
+    assert_scores_close(scores.cpu().numpy(), ref["scores"], "scores")
+    assert_anchors_match(anchors.cpu().numpy(), ref["scores"], w.K, "anchors")
+    a = anchors.cpu().numpy()
+    wp_ref, rs_ref = oracle.build_slot_maps(a, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+    assert np.array_equal(wp.cpu().numpy(), wp_ref) and np.array_equal(rs.cpu().numpy(), rs_ref)
+    kc0 = torch.zeros((lay.num_slots, w.hkv, w.d))
+    kc0[lay.shared_slot.long()] = inp["k_aff"]
+    vc0 = torch.zeros_like(kc0)
+    vc0[lay.shared_slot.long()] = inp["v_aff"]
+    kb, vb, flags = oracle.write_slots(lay.private_slots, rec["k_new"], rec["v_new"], kc0, vc0,
+                                       private_begin=lay.private_begin)
+    assert flags == 0
+    assert np.array_equal(kc.cpu().view(torch.uint8).reshape(-1).numpy(), kb)
+    assert np.array_equal(vc.cpu().view(torch.uint8).reshape(-1).numpy(), vb)
+    ref_o = oracle.slot_attention(rec["q_r"], rs_ref, kc.cpu(), vc.cpu(), scale=w.scale)
+    assert_out_close(out.cpu().numpy(), ref_o, "f32", "slot attention")
