@@ -61,7 +61,7 @@ def build(verbose: bool = False, extra=(), jobs: int | None = None) -> str:
         objs = list(ex.map(lambda s: _compile(s, list(extra), verbose), srcs))
     if _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-lcuda"]
+        cmd = [NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs,]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -34,6 +34,18 @@ struct SlotKeys {
         vr = v_cache + off;
         return true;
     }
+    // Element offset of key t's row (same for K and V) in source `src`, or -1 (zero row).
+    ACACHE_DEVFN int64_t locate(int b, int t, int hk, int& src, int32_t* dev_status) const {
+        src = 0;
+        const int64_t s = read_slot[(int64_t)b * T_len + t];
+        if (s < 0 || s >= num_slots) {
+            flag(dev_status, ACACHE_DEV_BAD_SLOT);
+            return -1;
+        }
+        return (s * hkv + hk) * d;
+    }
+    ACACHE_DEVFN const T* kbase(int) const { return k_cache; }
+    ACACHE_DEVFN const T* vbase(int) const { return v_cache; }
 };
 
 // Keys of the probe: logical key t is the shared affix row t - l for t in F = [l, l+L),
@@ -58,6 +70,18 @@ struct ProbeKeys {
         }
         return true;
     }
+    // source 0 = the shared affix cache, 1 = the request's own rows
+    ACACHE_DEVFN int64_t locate(int b, int t, int hk, int& src, int32_t*) const {
+        if (t >= l && t < l + L) {
+            src = 0;
+            return ((int64_t)(t - l) * hkv + hk) * d;
+        }
+        src = 1;
+        const int pr = t < l ? t : t - L;
+        return (((int64_t)b * P + pr) * hkv + hk) * d;
+    }
+    ACACHE_DEVFN const T* kbase(int src) const { return src ? k_req : k_aff; }
+    ACACHE_DEVFN const T* vbase(int src) const { return src ? v_req : v_aff; }
 };
 
 // ---- launchers (host) ---------------------------------------------------------------

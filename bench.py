@@ -42,6 +42,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle sample")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run this many layers instead of the workload's")
+    ap.add_argument("--points", type=int, default=0,
+                    help="profiling only: recompute points per step instead of the workload's")
     return ap.parse_args()
 
 
@@ -315,6 +319,10 @@ def run_reference(args, w, world, rank):
 def main():
     args = parse()
     w = wl.CATALOGUE[args.workload]
+    if args.layers:
+        w = w.replace(layers=args.layers)
+    if args.points:
+        w = w.replace(recompute_points=args.points)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, w, world, rank)

@@ -261,12 +261,32 @@ def test_slot_attention_bad_slot_reads_zero_row():
 
 # ------------------------------------------------------------------ the tiny workload end to end
 def test_tiny_prefix_f32_pipeline():
-    """Probe -> scores -> Top-K(26) -> maps -> write 122 rows -> slot attention (122 x 224)."""
+    """Probe -> scores -> Top-K(26) -> maps -> write 122 rows -> slot attention (122 x 224).
+
+    The oracle runs its own chain from the generator's inputs; each GPU stage is compared
+    with the oracle's stage.  No GPU result is fed to the oracle."""
     w = wl.TINY_PREFIX_F32
     lay = wl.slot_layout(w)
     inp = wl.probe_inputs(w, 0)
+    rec = wl.recompute_inputs(w, 0)
+    # ---- oracle chain
     ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
                              T=w.T, l=w.l, masked_rows=w.masked_rows(), scale=w.scale)
+    a_ref = oracle.topk_anchors(ref["scores"], w.K)
+    wp_ref, rs_ref = oracle.build_slot_maps(a_ref, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+    kc0 = torch.zeros((lay.num_slots, w.hkv, w.d))
+    vc0 = torch.zeros_like(kc0)
+    kb, vb, _ = oracle.write_slots(lay.shared_slot[None], inp["k_aff"][None], inp["v_aff"][None],
+                                   kc0, vc0, private_begin=0)
+    kc0 = torch.from_numpy(kb).view(torch.float32).view(kc0.shape)
+    vc0 = torch.from_numpy(vb).view(torch.float32).view(vc0.shape)
+    kb, vb, flags = oracle.write_slots(lay.private_slots, rec["k_new"], rec["v_new"], kc0, vc0,
+                                       private_begin=lay.private_begin)
+    assert flags == 0
+    kc_ref = torch.from_numpy(kb).view(torch.float32).view(kc0.shape)
+    vc_ref = torch.from_numpy(vb).view(torch.float32).view(vc0.shape)
+    o_ref = oracle.slot_attention(rec["q_r"], rs_ref, kc_ref, vc_ref, scale=w.scale)
+    # ---- GPU chain
     scores = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
     o = probe_layer_gpu(w, inp, scores)
     anchors = torch.empty((w.batch, w.K), dtype=torch.int32, device="cuda")
@@ -278,28 +298,19 @@ def test_tiny_prefix_f32_pipeline():
     kc = torch.zeros((lay.num_slots, w.hkv, w.d), dtype=torch.float32, device="cuda")
     vc = torch.zeros_like(kc)
     register_shared(w, lay, inp["k_aff"], inp["v_aff"], kc, vc)
-    rec = wl.recompute_inputs(w, 0)
     ac.acache_write_slots(desc_of(w), w.batch, w.R, dev(lay.private_slots), dev(rec["k_new"]),
                           dev(rec["v_new"]), kc, vc, lay.num_slots, lay.private_begin)
     out = torch.empty((w.batch, w.R, w.hq, w.d), dtype=torch.float32, device="cuda")
     ac.acache_slot_attention(desc_of(w), w.batch, w.R, dev(rec["q_r"]), w.T, rs, kc, vc,
                              lay.num_slots, out)
     torch.cuda.synchronize()
-    # step by step against the oracle
+    # ---- stage by stage
     assert_out_close(o.cpu().numpy(), ref["out"], "f32", "probe output")
     assert_scores_close(scores.cpu().numpy(), ref["scores"], "scores")
     assert_anchors_match(anchors.cpu().numpy(), ref["scores"], w.K, "anchors")
-    a = anchors.cpu().numpy()
-    wp_ref, rs_ref = oracle.build_slot_maps(a, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+    # this seeded case has no near-tie at the K-th score, so the sets are identical and
+    # every later stage is compared bit for bit / within tolerance
+    assert np.array_equal(anchors.cpu().numpy(), a_ref)
     assert np.array_equal(wp.cpu().numpy(), wp_ref) and np.array_equal(rs.cpu().numpy(), rs_ref)
-    kc0 = torch.zeros((lay.num_slots, w.hkv, w.d))
-    kc0[lay.shared_slot.long()] = inp["k_aff"]
-    vc0 = torch.zeros_like(kc0)
-    vc0[lay.shared_slot.long()] = inp["v_aff"]
-    kb, vb, flags = oracle.write_slots(lay.private_slots, rec["k_new"], rec["v_new"], kc0, vc0,
-                                       private_begin=lay.private_begin)
-    assert flags == 0
-    assert np.array_equal(kc.cpu().view(torch.uint8).reshape(-1).numpy(), kb)
-    assert np.array_equal(vc.cpu().view(torch.uint8).reshape(-1).numpy(), vb)
-    ref_o = oracle.slot_attention(rec["q_r"], rs_ref, kc.cpu(), vc.cpu(), scale=w.scale)
-    assert_out_close(out.cpu().numpy(), ref_o, "f32", "slot attention")
+    assert torch.equal(kc.cpu(), kc_ref) and torch.equal(vc.cpu(), vc_ref)
+    assert_out_close(out.cpu().numpy(), o_ref, "f32", "slot attention")
