@@ -1,4 +1,4 @@
-// tc_attn.cu -- tensor-core (tcgen05 + TMEM) attention kernels for bf16, head_dim 128.
+// tc_attn.cu -- tensor-core (tcgen05 + TMEM, TMA-fed) attention kernels for bf16, head_dim 128.
 //
 // Page: "Affix Cache for Diffusion Large Language Models" -- Sec. 3.2 (the one-shot probe,
 // Eq. 4-5) and Sec. 4.3 / App. C.1 (attention that reads every logical key through the
@@ -9,10 +9,16 @@
 //                  (request, query head); 256 threads, 1 CTA per SM)
 //   warps 0-3  softmax + epilogue: thread r owns query row r (= TMEM lane r)
 //   warp  4    TMEM allocation and the single MMA-issuing thread
-//   warps 5-7  producers: warp 5+s gathers key tiles j = s, s+3, ... (128 keys x 256 B for
-//              K and for V) with 16-byte cp.async through the key source (the read-slot
-//              map, or the affix / own-row split of the probe) straight into the 128-byte-
-//              swizzled K-major layout tcgen05.mma reads; warp 5 also loads the Q tile.
+//   warps 5-7  TMA producers.  Read-slot keys: the 128 `tile::gather4` loads of a tile
+//              (4 rows x 64 columns of K or V each, rows resolved through the read-slot map)
+//              are spread over the 96 producer lanes, so the per-instruction issue cost is
+//              shared by 3 warps;
+//              probe keys: the affix rows and the request's own rows are contiguous per KV
+//              head, so warp 5 loads each tile with 4 tiled box loads.  All loads land in the
+//              128-byte-swizzled K-major layout tcgen05.mma reads and complete on the stage's
+//              mbarrier by byte count (warp 5 announces the bytes; a load that completes first
+//              leaves the count transiently negative, which the barrier allows).  Q is 2 tiled
+//              box loads.
 //   TMEM (512 columns): S double buffer [0,128) [128,256) (fp32), O [256,384) (fp32).
 //   Per key tile j:  S_j = Q K_j^T (SS MMA, M=N=128, K=128)  ->  softmax threads read S_j,
 //   exponentiate in base 2 against a lazily raised row maximum (the maximum only moves
@@ -20,19 +26,22 @@
 //   write P_j as packed bf16 back over S_j's columns  ->  O += P_j V_j (TS MMA, P from
 //   TMEM, V from shared memory as an MN-major operand).  S_{j+1} is issued before PV_j, so
 //   the tensor core works on the next tile while the softmax threads exponentiate.
-//   The kernel emits O / row-sum and, for the probe, the row statistics (max, sum) that
+//   The kernel emits O / row sum and, for the probe, the row statistics (max, sum) that
 //   the second probe pass needs to normalise probabilities exactly.
 //
 // tc_colsum_kernel  (second probe pass: masked-to-affix attention mass; one CTA per
 //                    (request, query head, 128 affix keys))
 //   D = K_affix_tile Q_masked_chunk^T (SS MMA, M = 128 affix keys, N = 128 masked rows);
-//   thread r owns affix key r and sums 2^(logit - m_k) / l_k over the masked rows k in
-//   ascending order -- a per-thread serial sum, so the result is deterministic and no
-//   cross-thread reduction is needed.
+//   masked query rows are gathered with `tile::gather4`; thread r owns affix key r and sums
+//   2^(logit - m_k) / l_k over the masked rows k in ascending order -- a per-thread serial
+//   sum, so the result is deterministic and no cross-thread reduction is needed.
 //
 // Every mbarrier wait is bounded (about a second); a wait that gives up raises a CTA-wide
-// abort flag and ACACHE_DEV_TIMEOUT, every role leaves its loop, in-flight copies and MMAs
-// are drained with bounded waits, and TMEM is freed before the CTA exits.
+// abort flag and ACACHE_DEV_TIMEOUT, every role leaves its loop, in-flight MMAs are drained
+// with a bounded wait, and TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "tc_attn.cuh"
 #include "ptx.cuh"
 
@@ -45,10 +54,14 @@ using bf16 = __nv_bfloat16;
 constexpr int kD = 128;                     // head dim
 constexpr int kBM = 128;                    // query rows per CTA
 constexpr int kBN = 128;                    // keys per tile
-constexpr int kStages = 3;                  // K+V stages (= producer warps)
+constexpr int kStages = 3;                  // K+V stages
 constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;
-constexpr int kThreads = (kProdWarp0 + kStages) * 32;
+constexpr int kProdWarp = 5;                // first producer warp
+constexpr int kProdWarps = 3;               // gather4 issue is spread over 3 warps (8 warps =
+                                            // 2 full warpgroups keeps 255 registers a thread)
+constexpr int kGathers = 4 * (kBN / 4);     // gather4 loads per tile (K/V x 2 column halves)
+constexpr int kGathersPerWarp = (kGathers + kProdWarps - 1) / kProdWarps;
+constexpr int kThreads = (kProdWarp + kProdWarps) * 32;
 constexpr uint32_t kTileBytes = kBN * kD * 2;     // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t kRegion = kBN * 128;           // 16 KB: 64 columns of a 128-row tile
 constexpr uint32_t kSmemBytes = kTileBytes * (1 + 2 * kStages) + 1024;
@@ -56,6 +69,24 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: P values stay below 2^8
 constexpr long long kBudget = 1LL << 31;          // cycles (~1 s) before a wait gives up
+
+enum KeyMode { kSlotKeys = 0, kProbeKeys = 1 };
+
+struct AttnParams {
+    CUtensorMap tm_q;     // 4-D [B][n_rows][Hq][d], box {64, 1, 128, 1}
+    CUtensorMap tm_k0;    // slot: 2-D pool [num_slots*Hkv][d], box {64, 1} (gather4)
+    CUtensorMap tm_v0;    // probe: 3-D affix [L][Hkv][d], box {64, 1, 128}
+    CUtensorMap tm_k1;    // probe: 4-D own rows [B][P][Hkv][d], box {64, 1, 128, 1}
+    CUtensorMap tm_v1;
+    const int32_t* read_slot;
+    bf16* out;
+    float* stat_m;
+    float* stat_l;
+    int32_t* dev_status;
+    int64_t num_slots;
+    int n_rows, Hq, Hkv, T_len, L, P;
+    float scale_log2;
+};
 
 struct AttnCtl {
     uint64_t q_full;
@@ -85,51 +116,43 @@ ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_f
     }
 }
 
-// Copy one 128-row x 128-column bf16 tile into the 128-byte-swizzled K-major layout.  Lane
-// l holds the location (source, element offset; offset -1 = zero row) of rows l, l+32,
-// l+64 and l+96, resolved up front with independent loads; every copy instruction moves two
-// whole 256-byte rows (lanes 0-15 one row, 16-31 the next) and takes the row's location
-// from its owner lane by shuffle.
-template <typename BaseFn>
-ACACHE_DEVFN void warp_copy_tile(uint32_t dst, int lane, const int64_t (&off)[4], const int (&src)[4],
-                                 BaseFn base_of, const bf16* fallback) {
-    const int ch = lane & 15;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-#pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-            const int owner = i * 2 + (lane >> 4);
-            const long long o = __shfl_sync(0xffffffffu, (long long)off[u], owner);
-            const int s = __shfl_sync(0xffffffffu, src[u], owner);
-            const bf16* p = o >= 0 ? base_of(s) + o + ch * 8 : fallback;
-            cp_async16(dst + sw128_offset(u * 32 + owner, ch, kBN), p, o >= 0 ? 16u : 0u);
-        }
-    }
+// Number of key tiles and the valid keys of tile j (identical on every role).  Probe tiles
+// cover the affix rows first, then the request's own rows: the order of keys inside a row
+// does not change the softmax.
+template <int kMode>
+ACACHE_DEVFN int n_key_tiles(const AttnParams& p) {
+    if (kMode == kSlotKeys) return (p.T_len + kBN - 1) / kBN;
+    return (p.L + kBN - 1) / kBN + (p.P + kBN - 1) / kBN;
+}
+template <int kMode>
+ACACHE_DEVFN int tile_valid(const AttnParams& p, int j) {
+    if (kMode == kSlotKeys) return min(kBN, p.T_len - j * kBN);
+    const int n_aff = (p.L + kBN - 1) / kBN;
+    return j < n_aff ? min(kBN, p.L - j * kBN) : min(kBN, p.P - (j - n_aff) * kBN);
 }
 
-template <typename Keys>
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, int n_rows, int Hq,
-               int Hkv, int T_len, float scale_log2, float* __restrict__ stat_m,
-               float* __restrict__ stat_l, int32_t* dev_status) {
+tc_attn_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t dsm[];
     __shared__ AttnCtl ctl;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     const uint32_t sQ = base;
-    const int n_qt = (n_rows + kBM - 1) / kBM;
+    const int n_qt = (p.n_rows + kBM - 1) / kBM;
     const int qt = blockIdx.x % n_qt;
-    const int h = (blockIdx.x / n_qt) % Hq;
-    const int b = blockIdx.x / (n_qt * Hq);
-    const int hk = h / (Hq / Hkv);
+    const int h = (blockIdx.x / n_qt) % p.Hq;
+    const int b = blockIdx.x / (n_qt * p.Hq);
+    const int hk = h / (p.Hq / p.Hkv);
     const int q0 = qt * kBM;
-    const int n_kv = (T_len + kBN - 1) / kBN;
+    const int n_kv = n_key_tiles<kMode>(p);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &ctl.abort;
+    int32_t* dev_status = p.dev_status;
 
     if (threadIdx.x == 0) {
-        mbar_init(&ctl.q_full, 32);
+        mbar_init(&ctl.q_full, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl.kv_full[s], 32);
+            mbar_init(&ctl.kv_full[s], 1);
             mbar_init(&ctl.kv_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -150,49 +173,89 @@ tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, in
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
-    if (warp >= kProdWarp0) {
-        // ------------------------------------------------------------------ producers
-        const int pw = warp - kProdWarp0;
-        if (pw == 0) {
-            int64_t off[4];
-            int src[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = q0 + u * 32 + lane;
-                src[u] = 0;
-                off[u] = i < n_rows ? (((int64_t)b * n_rows + i) * Hq + h) * kD : -1;
+    if (warp >= kProdWarp) {
+        // ------------------------------------------------------------------ TMA producers
+        const int pw = warp - kProdWarp;
+        if (pw == 0 && lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k0);
+            tma_prefetch_desc(&p.tm_v0);
+            if (kMode == kProbeKeys) {
+                tma_prefetch_desc(&p.tm_k1);
+                tma_prefetch_desc(&p.tm_v1);
             }
-            warp_copy_tile(sQ, lane, off, src, [&](int) { return q; }, q);
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&ctl.q_full);
+            mbar_arrive_expect_tx(&ctl.q_full, kTileBytes);
+            tma_load_4d(sQ, &p.tm_q, 0, h, q0, b, &ctl.q_full);
+            tma_load_4d(sQ + kRegion, &p.tm_q, 64, h, q0, b, &ctl.q_full);
         }
-        const uint32_t sK = base + kTileBytes * (1 + 2 * pw);
-        const uint32_t sV = sK + kTileBytes;
-        const bf16* fallback = q;
-        for (int j = pw; j < n_kv; j += kStages) {
-            // resolve the tile's 128 key rows first (independent loads), then wait for the stage
-            const int t0 = j * kBN;
-            int64_t off[4];
-            int src[4];
+        if (kMode == kProbeKeys && pw != 0) goto producers_done;
+        {
+            const int n_aff = (p.L + kBN - 1) / kBN;
+            const int oob_row = (int)(p.num_slots * p.Hkv);     // first row outside the pool
+            // read-slot keys: gather x (0..127) = 4-row group x / 4, kind x % 4 (0,1: K column
+            // halves; 2,3: V); warp pw issues x in [pw * kGathersPerWarp, ...) a lane at a time
+            const int x_end = min(kGathers, (pw + 1) * kGathersPerWarp);
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % kStages;
+                const uint32_t sK = base + kTileBytes * (1 + 2 * s);
+                const uint32_t sV = sK + kTileBytes;
+                int rows[2][4];
+                if (kMode == kSlotKeys) {
+                    // resolve the groups' rows through the read-slot map before waiting
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = t0 + u * 32 + lane;
-                src[u] = 0;
-                off[u] = t < T_len ? keys.locate(b, t, hk, src[u], dev_status) : -1;
+                    for (int e = 0; e < 2; ++e) {
+                        const int x = pw * kGathersPerWarp + lane + 32 * e;
+                        const int g = x >> 2;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int t = j * kBN + 4 * g + u;
+                            rows[e][u] = oob_row;
+                            if (x < x_end && t < p.T_len) {
+                                const int64_t slot = p.read_slot[(int64_t)b * p.T_len + t];
+                                if (slot >= 0 && slot < p.num_slots)
+                                    rows[e][u] = (int)(slot * p.Hkv + hk);
+                                else if ((x & 3) == 0)
+                                    flag(dev_status, ACACHE_DEV_BAD_SLOT);
+                            }
+                        }
+                    }
+                }
+                if (j >= kStages &&
+                    !__all_sync(0xffffffffu, wait_bar(&ctl.kv_empty[s], ((j / kStages) - 1) & 1,
+                                                      abort_flag, dev_status)))
+                    break;
+                if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&ctl.kv_full[s], 2 * kTileBytes);
+                __syncwarp();
+                if (kMode == kSlotKeys) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int x = pw * kGathersPerWarp + lane + 32 * e;
+                        if (x < x_end) {
+                            const int g = x >> 2, kind = x & 3;
+                            const uint32_t dst = (kind < 2 ? sK : sV) + (uint32_t)(kind & 1) * kRegion +
+                                                 (uint32_t)g * 512u;
+                            tma_gather4(dst, kind < 2 ? &p.tm_k0 : &p.tm_v0, (kind & 1) * 64, rows[e][0],
+                                        rows[e][1], rows[e][2], rows[e][3], &ctl.kv_full[s]);
+                        }
+                    }
+                } else if (lane == 0) {
+                    if (j < n_aff) {
+                        const int j0 = j * kBN;
+                        tma_load_3d(sK, &p.tm_k0, 0, hk, j0, &ctl.kv_full[s]);
+                        tma_load_3d(sK + kRegion, &p.tm_k0, 64, hk, j0, &ctl.kv_full[s]);
+                        tma_load_3d(sV, &p.tm_v0, 0, hk, j0, &ctl.kv_full[s]);
+                        tma_load_3d(sV + kRegion, &p.tm_v0, 64, hk, j0, &ctl.kv_full[s]);
+                    } else {
+                        const int r0 = (j - n_aff) * kBN;
+                        tma_load_4d(sK, &p.tm_k1, 0, hk, r0, b, &ctl.kv_full[s]);
+                        tma_load_4d(sK + kRegion, &p.tm_k1, 64, hk, r0, b, &ctl.kv_full[s]);
+                        tma_load_4d(sV, &p.tm_v1, 0, hk, r0, b, &ctl.kv_full[s]);
+                        tma_load_4d(sV + kRegion, &p.tm_v1, 64, hk, r0, b, &ctl.kv_full[s]);
+                    }
+                }
             }
-            if (j >= kStages &&
-                !wait_bar(&ctl.kv_empty[pw], ((j / kStages) - 1) & 1, abort_flag, dev_status))
-                break;
-            warp_copy_tile(sK, lane, off, src, [&](int s) { return keys.kbase(s); }, fallback);
-            warp_copy_tile(sV, lane, off, src, [&](int s) { return keys.vbase(s); }, fallback);
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&ctl.kv_full[pw]);
         }
-        cp_async_wait<0>();
+    producers_done:;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -244,6 +307,7 @@ tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, in
         // ------------------------------------------------------------------ softmax + epilogue
         const int r = threadIdx.x;                         // query row in the tile
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float c = p.scale_log2;                      // > 0
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
@@ -253,18 +317,25 @@ tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, in
             tc_fence_after();
             uint32_t v[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kColS + bs * kBN + c * 32, v[c]);
+            for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_base + kColS + bs * kBN + cc * 32, v[cc]);
             tmem_ld_wait();
-            const int valid = min(kBN, T_len - j * kBN);
-            float mt = -INFINITY;
+            const int valid = tile_valid<kMode>(p, j);
+            if (valid < kBN) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = (c * 32 + i < valid) ? __uint_as_float(v[c][i]) * scale_log2 : -INFINITY;
-                    v[c][i] = __float_as_uint(x);
-                    mt = fmaxf(mt, x);
-                }
+                    for (int i = 0; i < 32; ++i)
+                        if (cc * 32 + i >= valid) v[cc][i] = __float_as_uint(-INFINITY);
+            }
+            // row maximum of the raw logits (four independent chains)
+            float mx[4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                mx[cc] = __uint_as_float(v[cc][0]);
+#pragma unroll
+                for (int i = 1; i < 32; ++i) mx[cc] = fmaxf(mx[cc], __uint_as_float(v[cc][i]));
+            }
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
             float alpha = 1.f;
             bool resc = false;
             if (j == 0) {
@@ -280,28 +351,30 @@ tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, in
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int cc = 0; cc < 4; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + kColO + c * 32, o);
+                    tmem_ld32(lane_base + kColO + cc * 32, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(lane_base + kColO + c * 32, o);
+                    tmem_st32(lane_base + kColO + cc * 32, o);
                 }
                 tmem_st_wait();
             }
-            l_sum *= alpha;
+            const float neg_m = -m_used;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float p0 = fast_exp2(__uint_as_float(v[c][i]) - m_used);
-                    const float p1 = fast_exp2(__uint_as_float(v[c][i + 1]) - m_used);
-                    l_sum += p0 + p1;
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(v[cc][i]), c, neg_m));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(v[cc][i + 1]), c, neg_m));
+                    ls[cc] += p0 + p1;
                     __nv_bfloat162 two = __floats2bfloat162_rn(p0, p1);   // low half = lower key
-                    pk[c >> 1][(c & 1) * 16 + (i >> 1)] = *reinterpret_cast<uint32_t*>(&two);
+                    pk[cc >> 1][(cc & 1) * 16 + (i >> 1)] = *reinterpret_cast<uint32_t*>(&two);
                 }
+            l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
             // P_j (bf16 pairs, 64 columns) overwrites the first half of S_j's columns
             tmem_st32(lane_base + kColS + bs * kBN, pk[0]);
             tmem_st32(lane_base + kColS + bs * kBN + 32, pk[1]);
@@ -316,13 +389,13 @@ tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, in
             tc_fence_after();
             const int i = q0 + r;
             const float inv_l = 1.f / l_sum;
-            bf16* orow = out ? out + (((int64_t)b * n_rows + i) * Hq + h) * kD : nullptr;
+            bf16* orow = p.out ? p.out + (((int64_t)b * p.n_rows + i) * p.Hq + h) * kD : nullptr;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 4; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(lane_base + kColO + c * 32, o);
+                tmem_ld32(lane_base + kColO + cc * 32, o);
                 tmem_ld_wait();
-                if (orow && i < n_rows) {
+                if (orow && i < p.n_rows) {
                     uint32_t pkd[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
@@ -330,16 +403,16 @@ tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, in
                                                                    __uint_as_float(o[2 * x + 1]) * inv_l);
                         pkd[x] = *reinterpret_cast<uint32_t*>(&two);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
                     for (int x = 0; x < 4; ++x)
                         dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
                 }
             }
-            if (stat_m && i < n_rows) {
-                const int64_t so = ((int64_t)b * Hq + h) * n_rows + i;
-                stat_m[so] = m_used;
-                stat_l[so] = l_sum;
+            if (p.stat_m && i < p.n_rows) {
+                const int64_t so = ((int64_t)b * p.Hq + h) * p.n_rows + i;
+                p.stat_m[so] = m_used;
+                p.stat_l[so] = l_sum;
             }
         }
     }
@@ -352,9 +425,21 @@ tc_attn_kernel(Keys keys, const bf16* __restrict__ q, bf16* __restrict__ out, in
 // ------------------------------------------------------------------------------------------
 // Second probe pass.
 constexpr int kCsStages = 2;
-constexpr int kCsThreads = (kProdWarp0 + kCsStages) * 32;
+constexpr int kCsThreads = (kProdWarp + 1) * 32;   // one producer warp
 constexpr uint32_t kCsSmemBytes = kTileBytes * (1 + kCsStages) + 1024;
 constexpr uint32_t kCsTmemCols = 256;
+
+struct ColsumParams {
+    CUtensorMap tm_kaff;  // 3-D affix keys [L][Hkv][d], box {64, 1, 128}
+    CUtensorMap tm_q;     // 2-D probe queries [B*P*Hq][d], box {64, 1} (gather4)
+    const int32_t* masked;
+    const float* stat_m;
+    const float* stat_l;
+    float* partial;
+    int32_t* dev_status;
+    int B, P, L, m, Hq, Hkv;
+    float scale_log2;
+};
 
 struct ColsumCtl {
     uint64_t a_full;
@@ -370,27 +455,24 @@ struct ColsumCtl {
 };
 
 __global__ void __launch_bounds__(kCsThreads, 1)
-tc_colsum_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k_aff,
-                 const int32_t* __restrict__ masked, int P, int L, int m, int Hq, int Hkv,
-                 float scale_log2, const float* __restrict__ stat_m,
-                 const float* __restrict__ stat_l, float* __restrict__ partial,
-                 int32_t* dev_status) {
+tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     extern __shared__ uint8_t dsm[];
     __shared__ ColsumCtl ctl;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     const uint32_t sA = base;
-    const int n_jt = (L + kBN - 1) / kBN;
+    const int n_jt = (p.L + kBN - 1) / kBN;
     const int jt = blockIdx.x % n_jt;
-    const int h = (blockIdx.x / n_jt) % Hq;
-    const int b = blockIdx.x / (n_jt * Hq);
-    const int hk = h / (Hq / Hkv);
+    const int h = (blockIdx.x / n_jt) % p.Hq;
+    const int b = blockIdx.x / (n_jt * p.Hq);
+    const int hk = h / (p.Hq / p.Hkv);
     const int j0 = jt * kBN;
-    const int n_ch = (m + kBN - 1) / kBN;
+    const int n_ch = (p.m + kBN - 1) / kBN;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &ctl.abort;
+    int32_t* dev_status = p.dev_status;
 
     if (threadIdx.x == 0) {
-        mbar_init(&ctl.a_full, 32);
+        mbar_init(&ctl.a_full, 1);
         for (int s = 0; s < kCsStages; ++s) {
             mbar_init(&ctl.b_full[s], 32);
             mbar_init(&ctl.b_empty[s], 1);
@@ -411,56 +493,55 @@ tc_colsum_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k_aff,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
-    const float* sm_row = stat_m + ((int64_t)b * Hq + h) * P;
-    const float* sl_row = stat_l + ((int64_t)b * Hq + h) * P;
-    const int32_t* mrow = masked + (int64_t)b * m;
 
-    if (warp >= kProdWarp0) {
-        const int pw = warp - kProdWarp0;
-        if (pw == 0) {
-            int64_t off[4];
-            int src[4];
+    if (warp == kProdWarp) {
+        const float* sm_row = p.stat_m + ((int64_t)b * p.Hq + h) * p.P;
+        const float* sl_row = p.stat_l + ((int64_t)b * p.Hq + h) * p.P;
+        const int32_t* mrow = p.masked + (int64_t)b * p.m;
+        const int oob_row = p.B * p.P * p.Hq;               // first row outside the queries
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_kaff);
+            tma_prefetch_desc(&p.tm_q);
+            mbar_arrive_expect_tx(&ctl.a_full, kTileBytes);
+            tma_load_3d(sA, &p.tm_kaff, 0, hk, j0, &ctl.a_full);
+            tma_load_3d(sA + kRegion, &p.tm_kaff, 64, hk, j0, &ctl.a_full);
+        }
+        for (int c = 0; c < n_ch; ++c) {
+            const int s = c % kCsStages;
+            const uint32_t sB = base + kTileBytes * (1 + s);
+            int rows[4];
+            float sm[4], sil[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u * 32 + lane;
-                src[u] = 0;
-                off[u] = j < L ? ((int64_t)j * Hkv + hk) * kD : -1;
+                const int k = c * kBN + 4 * lane + u;
+                const int pr = k < p.m ? mrow[k] : -1;
+                const bool good = pr >= 0 && pr < p.P;
+                if (k < p.m && !good) flag(dev_status, ACACHE_DEV_BAD_ROW);
+                rows[u] = good ? ((b * p.P + pr) * p.Hq + h) : oob_row;
+                sm[u] = good ? sm_row[pr] : INFINITY;
+                sil[u] = good ? 1.f / sl_row[pr] : 0.f;
             }
-            warp_copy_tile(sA, lane, off, src, [&](int) { return k_aff; }, k_aff);
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&ctl.a_full);
-        }
-        const uint32_t sB = base + kTileBytes * (1 + pw);
-        for (int c = pw; c < n_ch; c += kCsStages) {
             if (c >= kCsStages) {
                 const uint32_t par = ((c / kCsStages) - 1) & 1;
-                if (!wait_bar(&ctl.b_empty[pw], par, abort_flag, dev_status)) break;
-                if (!wait_bar(&ctl.cons_done[pw], par, abort_flag, dev_status)) break;
+                if (!__all_sync(0xffffffffu, wait_bar(&ctl.b_empty[s], par, abort_flag, dev_status) &&
+                                                 wait_bar(&ctl.cons_done[s], par, abort_flag, dev_status)))
+                    break;
             }
-            const int k0 = c * kBN;
-            int64_t off[4];
-            int src[4];
+            // every lane stores its rows' statistics before its arrival on b_full publishes
+            // them (lane 0 arrives through the expect_tx that announces the chunk's bytes,
+            // before any lane issues its loads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int row = u * 32 + lane;
-                const int k = k0 + row;
-                const int p = k < m ? mrow[k] : -1;
-                const bool good = p >= 0 && p < P;
-                if (k < m && !good) flag(dev_status, ACACHE_DEV_BAD_ROW);
-                src[u] = 0;
-                off[u] = good ? (((int64_t)b * P + p) * Hq + h) * kD : -1;
-                ctl.st_m[pw][row] = good ? sm_row[p] : INFINITY;
-                ctl.st_il[pw][row] = good ? 1.f / sl_row[p] : 0.f;
+                ctl.st_m[s][4 * lane + u] = sm[u];
+                ctl.st_il[s][4 * lane + u] = sil[u];
             }
-            warp_copy_tile(sB, lane, off, src, [&](int) { return q; }, q);
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&ctl.b_full[pw]);
+            if (lane == 0) mbar_arrive_expect_tx(&ctl.b_full[s], kTileBytes);
+            __syncwarp();
+            const uint32_t o = (uint32_t)lane * 512u;
+            tma_gather4(sB + o, &p.tm_q, 0, rows[0], rows[1], rows[2], rows[3], &ctl.b_full[s]);
+            tma_gather4(sB + kRegion + o, &p.tm_q, 64, rows[0], rows[1], rows[2], rows[3], &ctl.b_full[s]);
+            if (lane != 0) mbar_arrive(&ctl.b_full[s]);
         }
-        cp_async_wait<0>();
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             const uint32_t id = idesc_bf16(kBN, kBN, false, false);
@@ -488,6 +569,7 @@ tc_colsum_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k_aff,
     } else {
         const int r = threadIdx.x;                         // affix key j0 + r
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float c2 = p.scale_log2;
         float acc = 0.f;
         bool ok = true;
         for (int c = 0; c < n_ch; ++c) {
@@ -506,13 +588,13 @@ tc_colsum_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k_aff,
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int k = cc * 32 + i;
-                    acc += fast_exp2(__uint_as_float(v[i]) * scale_log2 - ctl.st_m[s][k]) * ctl.st_il[s][k];
+                    acc += fast_exp2(fmaf(__uint_as_float(v[i]), c2, -ctl.st_m[s][k])) * ctl.st_il[s][k];
                 }
             }
             tc_fence_before();
             mbar_arrive(&ctl.cons_done[db]);
         }
-        if (ok && j0 + r < L) partial[((int64_t)b * Hq + h) * L + j0 + r] = acc;
+        if (ok && j0 + r < p.L) p.partial[((int64_t)b * p.Hq + h) * p.L + j0 + r] = acc;
     }
     tc_fence_before();
     __syncthreads();
@@ -520,52 +602,124 @@ tc_colsum_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k_aff,
     if (warp == kMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
 }
 
-template <typename Keys>
-int launch_attn(Keys keys, const void* q, void* out, int B, int n_rows, int Hq, int Hkv, int T_len,
-                float scale_log2, float* stat_m, float* stat_l, int32_t* dev_status,
-                cudaStream_t stream) {
-    const int64_t ctas = (int64_t)B * Hq * ((n_rows + kBM - 1) / kBM);
+// ---- host: tensor maps -----------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
+
+// bf16 tensor of `rank` dims (innermost first, dims[0] = head_dim), 128-byte swizzle, box
+// {64, 1, ..., box_rows at dimension `row_dim`, 1, ...}; out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, int row_dim,
+              uint32_t box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t box[5], estr[5];
+    uint64_t stride = 2;
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i] ? dims[i] : 1;
+        if (i > 0) gstride[i - 1] = stride;
+        stride *= gdim[i];
+        box[i] = 1;
+        estr[i] = 1;
+    }
+    box[0] = 64;
+    box[row_dim] = box_rows;
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gdim, gstride, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kMode>
+int launch_attn(const AttnParams& prm, int B, cudaStream_t stream) {
+    const int64_t ctas = (int64_t)B * prm.Hq * ((prm.n_rows + kBM - 1) / kBM);
     if (ctas == 0) return ACACHE_OK;
     if (ctas > 0x7fffffff) return ACACHE_ERR_INVALID_ARG;
-    auto kern = tc_attn_kernel<Keys>;
+    auto kern = tc_attn_kernel<kMode>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
     }
-    kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(keys, (const bf16*)q, (bf16*)out, n_rows, Hq,
-                                                         Hkv, T_len, scale_log2, stat_m, stat_l,
-                                                         dev_status);
+    kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(prm);
     return launch_status();
 }
 
 }  // namespace
 
-bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == kD; }
+bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == kD && a.scale > 0.f; }
 
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
                              cudaStream_t stream) {
-    SlotKeys<bf16> keys{(const bf16*)k_cache, (const bf16*)v_cache, read_slot, num_slots, T_len,
-                        a.hkv, kD};
-    return launch_attn(keys, q, out, B, n_q, a.hq, a.hkv, T_len, a.scale * kLog2e, nullptr, nullptr,
-                       dev_status, stream);
+    if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
+        return ACACHE_ERR_INVALID_ARG;
+    AttnParams prm{};
+    const uint64_t dq[4] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)n_q, (uint64_t)B};
+    const uint64_t dp[2] = {(uint64_t)kD, (uint64_t)num_slots * a.hkv};
+    if (!make_map(&prm.tm_q, q, 4, dq, 2, kBM) || !make_map(&prm.tm_k0, k_cache, 2, dp, 1, 1) ||
+        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1))
+        return ACACHE_ERR_CUDA;
+    prm.tm_k1 = prm.tm_k0;
+    prm.tm_v1 = prm.tm_v0;
+    prm.read_slot = read_slot;
+    prm.out = (bf16*)out;
+    prm.dev_status = dev_status;
+    prm.num_slots = num_slots;
+    prm.n_rows = n_q;
+    prm.Hq = a.hq;
+    prm.Hkv = a.hkv;
+    prm.T_len = T_len;
+    prm.scale_log2 = a.scale * kLog2e;
+    return launch_attn<kSlotKeys>(prm, B, stream);
 }
 
 int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                            const void* k_req, const void* v_req, const void* k_aff,
                            const void* v_aff, void* out, float* stat_m, float* stat_l,
                            int32_t* dev_status, cudaStream_t stream) {
-    ProbeKeys<bf16> keys{(const bf16*)k_req, (const bf16*)v_req, (const bf16*)k_aff,
-                         (const bf16*)v_aff, l, L, T_len - L, a.hkv, kD};
-    return launch_attn(keys, q, out, B, T_len - L, a.hq, a.hkv, T_len, a.scale * kLog2e, stat_m,
-                       stat_l, dev_status, stream);
+    (void)l;   // key order inside a row does not change the softmax: affix tiles, then own tiles
+    const int P = T_len - L;
+    AttnParams prm{};
+    const uint64_t dq[4] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)P, (uint64_t)B};
+    const uint64_t da[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)L};
+    const uint64_t dr[4] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)P, (uint64_t)B};
+    const void* ka = L > 0 ? k_aff : k_req;   // an unused map still needs a valid address
+    const void* va = L > 0 ? v_aff : v_req;
+    if (!make_map(&prm.tm_q, q, 4, dq, 2, kBM) || !make_map(&prm.tm_k0, ka, 3, da, 2, kBN) ||
+        !make_map(&prm.tm_v0, va, 3, da, 2, kBN) || !make_map(&prm.tm_k1, k_req, 4, dr, 2, kBN) ||
+        !make_map(&prm.tm_v1, v_req, 4, dr, 2, kBN))
+        return ACACHE_ERR_CUDA;
+    prm.out = (bf16*)out;
+    prm.stat_m = stat_m;
+    prm.stat_l = stat_l;
+    prm.dev_status = dev_status;
+    prm.n_rows = P;
+    prm.Hq = a.hq;
+    prm.Hkv = a.hkv;
+    prm.T_len = T_len;
+    prm.L = L;
+    prm.P = P;
+    prm.scale_log2 = a.scale * kLog2e;
+    return launch_attn<kProbeKeys>(prm, B, stream);
 }
 
 int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int32_t* masked_rows,
                            int m, const void* q, const void* k_aff, const float* stat_m,
                            const float* stat_l, float* partial, int32_t* dev_status,
                            cudaStream_t stream) {
+    const int P = T_len - L;
     const int64_t ctas = (int64_t)B * a.hq * ((L + kBN - 1) / kBN);
     if (ctas == 0) return ACACHE_OK;
     if (m == 0) {   // no masked rows: every affix key receives zero mass
@@ -573,14 +727,30 @@ int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int
             return ACACHE_ERR_CUDA;
         return ACACHE_OK;
     }
+    if ((int64_t)B * P * a.hq >= 0x7fffffffLL) return ACACHE_ERR_INVALID_ARG;
+    ColsumParams prm{};
+    const uint64_t da[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)L};
+    const uint64_t dq[2] = {(uint64_t)kD, (uint64_t)B * P * a.hq};
+    if (!make_map(&prm.tm_kaff, k_aff, 3, da, 2, kBN) || !make_map(&prm.tm_q, q, 2, dq, 1, 1))
+        return ACACHE_ERR_CUDA;
+    prm.masked = masked_rows;
+    prm.stat_m = stat_m;
+    prm.stat_l = stat_l;
+    prm.partial = partial;
+    prm.dev_status = dev_status;
+    prm.B = B;
+    prm.P = P;
+    prm.L = L;
+    prm.m = m;
+    prm.Hq = a.hq;
+    prm.Hkv = a.hkv;
+    prm.scale_log2 = a.scale * kLog2e;
     if (cudaFuncSetAttribute(tc_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kCsSmemBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
     }
-    tc_colsum_kernel<<<(unsigned)ctas, kCsThreads, kCsSmemBytes, stream>>>(
-        (const bf16*)q, (const bf16*)k_aff, masked_rows, T_len - L, L, m, a.hq, a.hkv,
-        a.scale * kLog2e, stat_m, stat_l, partial, dev_status);
+    tc_colsum_kernel<<<(unsigned)ctas, kCsThreads, kCsSmemBytes, stream>>>(prm);
     return launch_status();
 }
 
