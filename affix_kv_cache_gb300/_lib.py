@@ -27,7 +27,7 @@ ACACHE_BF16 = 1
 DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
 
 EXPORTS = ("acache_status_string", "acache_version", "acache_probe_workspace_bytes",
-           "acache_probe_scores", "acache_topk_anchors", "acache_build_slot_maps",
+           "acache_probe_scores", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
            "acache_write_slots", "acache_slot_attention", "acache_gather_slots")
 
 
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "acache_version": (I, []),
             "acache_probe_workspace_bytes": (S, [D, I, I, I, I]),
             "acache_probe_scores": (I, [D, I, I, I, I, P, I, P, P, P, P, P, P, P, P, S, P, P]),
+            "acache_probe_scores_noalloc": (I, [D, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P]),
             "acache_topk_anchors": (I, [P, I, I, I, P, P, P]),
             "acache_build_slot_maps": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
             "acache_write_slots": (I, [D, I, I, P, P, P, P, P, I64, I64, P, P]),
@@ -127,6 +128,18 @@ def acache_probe_scores(desc, batch, seq_len, affix_begin, affix_len, masked_row
                                    _p(k_affix), _p(v_affix), _p(out), _p(scores), _p(workspace),
                                    workspace_bytes, _p(dev_status), _stream(stream))
     return _check("acache_probe_scores", st) if check else st
+
+
+def acache_probe_scores_noalloc(desc, batch, seq_len, affix_begin, affix_len, masked_rows,
+                                num_masked, q, k_req, v_req, k_affix, v_affix, out, scores,
+                                dev_status=None, stream=None, check=True):
+    """acache_probe_scores without a workspace, for callers that cannot allocate device
+    memory: the scratch is a fixed 16 MiB array inside the library (see include/acache.h)."""
+    st = lib().acache_probe_scores_noalloc(ctypes.byref(desc), batch, seq_len, affix_begin,
+                                           affix_len, _p(masked_rows), num_masked, _p(q),
+                                           _p(k_req), _p(v_req), _p(k_affix), _p(v_affix),
+                                           _p(out), _p(scores), _p(dev_status), _stream(stream))
+    return _check("acache_probe_scores_noalloc", st) if check else st
 
 
 def acache_topk_anchors(scores, batch, affix_len, k, anchors, dev_status=None, stream=None,

@@ -115,6 +115,30 @@ ACACHE_API int acache_probe_scores(const acache_attn_desc* a, int batch, int seq
                         void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * Probe without a workspace.  The page has no counterpart: this entry point exists for
+ * callers that cannot allocate device memory when they probe -- an engine that gives the
+ * library only tensors it already owns (a memory budget split up at start-up, an allocator
+ * the library cannot reach, or code that must not enter the CUDA allocator).
+ *
+ * Same computation, arguments, layouts and errors as acache_probe_scores, minus the
+ * workspace: the scratch (row maximum and sum, per-head column sums) lives in one fixed
+ * 16 MiB device array inside the library, reserved on every GPU that loads it until the
+ * process exits.  A call needing more than that (2 * round256(B*Hq*P*4) +
+ * round256(B*Hq*L*4) bytes) returns ACACHE_ERR_WORKSPACE and launches nothing.  The call
+ * allocates nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ *  - The first call on a device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture starts.
+ *  - All calls share the array and it keeps the last call's contents.  Nothing in it must
+ *    start at zero (each call writes every scratch byte it reads), but calls whose kernels
+ *    can overlap on the GPU (unordered streams) race on it: order them.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_probe_scores_noalloc(const acache_attn_desc* a, int batch, int seq_len,
+                        int affix_begin, int affix_len, const int32_t* masked_rows,
+                        int num_masked, const void* q, const void* k_req, const void* v_req,
+                        const void* k_affix, const void* v_affix, void* out, float* scores,
+                        int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * (3) Anchor selection.  Page: Sec. 3.2, Eq. 6, A = TopK({s_j}, K), S = F \ A.
  * anchors[b] receives the K affix offsets with the largest scores, ties broken toward the
  * lower offset, written in ascending offset order.  -0.0 counts as +0.0.  A NaN score
