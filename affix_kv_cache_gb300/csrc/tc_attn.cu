@@ -52,21 +52,28 @@ using namespace ptx;
 using bf16 = __nv_bfloat16;
 
 constexpr int kD = 128;                     // head dim
-constexpr int kBM = 128;                    // query rows per CTA
+constexpr int kBM = 128;                    // query rows per Q tile (one softmax warpgroup)
+constexpr int kQT = 2;                      // Q tiles per CTA: 256 query rows share each K/V tile
 constexpr int kBN = 128;                    // keys per tile
-constexpr int kStages = 3;                  // K+V stages
-constexpr int kMmaWarp = 4;
-constexpr int kProdWarp = 5;                // first producer warp
-constexpr int kProdWarps = 3;               // gather4 issue is spread over 3 warps (8 warps =
-                                            // 2 full warpgroups keeps 255 registers a thread)
-constexpr int kGathers = 4 * (kBN / 4);     // gather4 loads per tile (K/V x 2 column halves)
-constexpr int kGathersPerWarp = (kGathers + kProdWarps - 1) / kProdWarps;
-constexpr int kThreads = (kProdWarp + kProdWarps) * 32;
+constexpr int kKStages = 3;                 // K ring: a K tile is free once S_B has read it
+constexpr int kVStages = 2;                 // V ring: a V tile is free once PV_B has read it
+constexpr int kMmaWarp = 8;                 // warpgroup 2: TMEM allocation + the MMA thread
+constexpr int kProdWarp = 12;               // warpgroup 3: the 4 TMA producer warps
+constexpr int kProdWarps = 4;               // one per SM sub-partition: gather4 issue runs in
+                                            // parallel on the four of them
+constexpr int kThreads = 16 * 32;
+// Registers: 512 threads x 128 at launch = 65536; the softmax warpgroups grow to 200, the
+// MMA / producer warpgroups shrink to 56: 2*128*200 + 2*128*56 = 65536.
+constexpr int kRegSoftmax = 200, kRegOther = 56;
+static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther <= kThreads * 128, "register split");
+constexpr int kGathersPerWarp = 4 * (kBN / 4) / kProdWarps;   // 32: one gather4 per lane
+                                                               // (warps 12-13: K, 14-15: V)
 constexpr uint32_t kTileBytes = kBN * kD * 2;     // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t kRegion = kBN * 128;           // 16 KB: 64 columns of a 128-row tile
-constexpr uint32_t kSmemBytes = kTileBytes * (1 + 2 * kStages) + 1024;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;
+constexpr uint32_t kSmemBytes = kTileBytes * (kQT + kKStages + kVStages) + 1024;
+constexpr uint32_t kTmemCols = 512;               // S_A, S_B, O_A, O_B: 128 fp32 columns each
+__host__ __device__ constexpr uint32_t col_s(int t) { return (uint32_t)t * 128u; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + (uint32_t)t * 128u; }
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: P values stay below 2^8
 constexpr long long kBudget = 1LL << 31;          // cycles (~1 s) before a wait gives up
 
@@ -90,11 +97,12 @@ struct AttnParams {
 
 struct AttnCtl {
     uint64_t q_full;
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t o_done;
+    uint64_t k_full[kKStages];
+    uint64_t k_empty[kKStages];
+    uint64_t v_full[kVStages];
+    uint64_t v_empty[kVStages];
+    uint64_t s_full[kQT];
+    uint64_t p_full[kQT];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -137,29 +145,36 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t dsm[];
     __shared__ AttnCtl ctl;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
-    const uint32_t sQ = base;
-    const int n_qt = (p.n_rows + kBM - 1) / kBM;
-    const int qt = blockIdx.x % n_qt;
-    const int h = (blockIdx.x / n_qt) % p.Hq;
-    const int b = blockIdx.x / (n_qt * p.Hq);
+    // shared memory: Q_A, Q_B, the K ring, the V ring (32 KB tiles, 1024-byte aligned)
+    auto sQ = [&](int t) { return base + kTileBytes * (uint32_t)t; };
+    auto sK = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + s); };
+    auto sV = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + kKStages + s); };
+    const int n_qb = (p.n_rows + kQT * kBM - 1) / (kQT * kBM);
+    const int qb = blockIdx.x % n_qb;
+    const int h = (blockIdx.x / n_qb) % p.Hq;
+    const int b = blockIdx.x / (n_qb * p.Hq);
     const int hk = h / (p.Hq / p.Hkv);
-    const int q0 = qt * kBM;
+    const int q0 = qb * kQT * kBM;
+    const int n_qt = min(kQT, (p.n_rows - q0 + kBM - 1) / kBM);   // Q tiles present (1 or 2)
     const int n_kv = n_key_tiles<kMode>(p);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl.kv_full[s], 1);
-            mbar_init(&ctl.kv_empty[s], 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&ctl.k_full[s], 1);
+            mbar_init(&ctl.k_empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl.s_full[i], 1);
-            mbar_init(&ctl.p_full[i], 128);
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&ctl.v_full[s], 1);
+            mbar_init(&ctl.v_empty[s], 1);
         }
-        mbar_init(&ctl.o_done, 1);
+        for (int t = 0; t < kQT; ++t) {
+            mbar_init(&ctl.s_full[t], 1);
+            mbar_init(&ctl.p_full[t], 128);
+        }
         mbar_init(&ctl.drain, 1);
         ctl.abort = 0;
         fence_mbar_init();
@@ -173,8 +188,11 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
-    if (warp >= kProdWarp) {
+    // Each role's code sits inside the branch of its register reallocation, so the compiler
+    // allocates every region against the right register limit.
+    if (wg == 3) {
         // ------------------------------------------------------------------ TMA producers
+        setmaxnreg_dec<kRegOther>();
         const int pw = warp - kProdWarp;
         if (pw == 0 && lane == 0) {
             tma_prefetch_desc(&p.tm_q);
@@ -184,140 +202,158 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 tma_prefetch_desc(&p.tm_k1);
                 tma_prefetch_desc(&p.tm_v1);
             }
-            mbar_arrive_expect_tx(&ctl.q_full, kTileBytes);
-            tma_load_4d(sQ, &p.tm_q, 0, h, q0, b, &ctl.q_full);
-            tma_load_4d(sQ + kRegion, &p.tm_q, 64, h, q0, b, &ctl.q_full);
+            mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_qt);
+            for (int t = 0; t < n_qt; ++t) {
+                tma_load_4d(sQ(t), &p.tm_q, 0, h, q0 + t * kBM, b, &ctl.q_full);
+                tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, h, q0 + t * kBM, b, &ctl.q_full);
+            }
         }
-        if (kMode == kProbeKeys && pw != 0) goto producers_done;
-        {
+        // warps 12-13 fill the K ring, warps 14-15 the V ring; probe tiles are box loads
+        // issued by lane 0 of warps 12 (K) and 14 (V)
+        const bool is_v = pw >= 2;
+        const int nst = is_v ? kVStages : kKStages;
+        uint64_t* full = is_v ? ctl.v_full : ctl.k_full;
+        uint64_t* empty = is_v ? ctl.v_empty : ctl.k_empty;
+        const CUtensorMap* tm_aff = is_v ? &p.tm_v0 : &p.tm_k0;   // slot: the pool
+        const CUtensorMap* tm_own = is_v ? &p.tm_v1 : &p.tm_k1;
+        const bool leader = (pw & 1) == 0 && lane == 0;            // announces the tile's bytes
+        if (kMode == kSlotKeys || (pw & 1) == 0) {
             const int n_aff = (p.L + kBN - 1) / kBN;
             const int oob_row = (int)(p.num_slots * p.Hkv);     // first row outside the pool
-            // read-slot keys: gather x (0..127) = 4-row group x / 4, kind x % 4 (0,1: K column
-            // halves; 2,3: V); warp pw issues x in [pw * kGathersPerWarp, ...) a lane at a time
-            const int x_end = min(kGathers, (pw + 1) * kGathersPerWarp);
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % kStages;
-                const uint32_t sK = base + kTileBytes * (1 + 2 * s);
-                const uint32_t sV = sK + kTileBytes;
-                int rows[2][4];
-                if (kMode == kSlotKeys) {
-                    // resolve the groups' rows through the read-slot map before waiting
+            // read-slot keys: this lane's gather x = 4-row group x / 2 of the tile, column
+            // half x % 2 of the warp pair's matrix (K or V)
+            const int x = (pw & 1) * 32 + lane;
+            const int g = x >> 1, half = x & 1;
+            // rows of tile j are resolved one iteration ahead, so the read-slot loads overlap
+            // the previous tile's wait and gather issue
+            auto resolve = [&](int j, int (&rows)[4]) {
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int x = pw * kGathersPerWarp + lane + 32 * e;
-                        const int g = x >> 2;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int t = j * kBN + 4 * g + u;
-                            rows[e][u] = oob_row;
-                            if (x < x_end && t < p.T_len) {
-                                const int64_t slot = p.read_slot[(int64_t)b * p.T_len + t];
-                                if (slot >= 0 && slot < p.num_slots)
-                                    rows[e][u] = (int)(slot * p.Hkv + hk);
-                                else if ((x & 3) == 0)
-                                    flag(dev_status, ACACHE_DEV_BAD_SLOT);
-                            }
-                        }
+                for (int u = 0; u < 4; ++u) {
+                    const int t = j * kBN + 4 * g + u;
+                    rows[u] = oob_row;
+                    if (kMode == kSlotKeys && j < n_kv && t < p.T_len) {
+                        const int64_t slot = p.read_slot[(int64_t)b * p.T_len + t];
+                        if (slot >= 0 && slot < p.num_slots)
+                            rows[u] = (int)(slot * p.Hkv + hk);
+                        else if (!is_v && half == 0)
+                            flag(dev_status, ACACHE_DEV_BAD_SLOT);
                     }
                 }
-                if (j >= kStages &&
-                    !__all_sync(0xffffffffu, wait_bar(&ctl.kv_empty[s], ((j / kStages) - 1) & 1,
-                                                      abort_flag, dev_status)))
+            };
+            int next[4];
+            resolve(0, next);
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % nst;
+                const uint32_t dst_tile = is_v ? sV(s) : sK(s);
+                int rows[4] = {next[0], next[1], next[2], next[3]};
+                resolve(j + 1, next);
+                if (j >= nst &&
+                    !__all_sync(0xffffffffu, wait_bar(&empty[s], ((j / nst) - 1) & 1, abort_flag,
+                                                      dev_status)))
                     break;
-                if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&ctl.kv_full[s], 2 * kTileBytes);
+                // the warp pair's first warp announces the tile's bytes; a gather of the other
+                // warp that completes first leaves the count transiently negative (allowed)
+                if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
                 __syncwarp();
                 if (kMode == kSlotKeys) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int x = pw * kGathersPerWarp + lane + 32 * e;
-                        if (x < x_end) {
-                            const int g = x >> 2, kind = x & 3;
-                            const uint32_t dst = (kind < 2 ? sK : sV) + (uint32_t)(kind & 1) * kRegion +
-                                                 (uint32_t)g * 512u;
-                            tma_gather4(dst, kind < 2 ? &p.tm_k0 : &p.tm_v0, (kind & 1) * 64, rows[e][0],
-                                        rows[e][1], rows[e][2], rows[e][3], &ctl.kv_full[s]);
-                        }
-                    }
+                    tma_gather4(dst_tile + (uint32_t)half * kRegion + (uint32_t)g * 512u, tm_aff, half * 64,
+                                rows[0], rows[1], rows[2], rows[3], &full[s]);
                 } else if (lane == 0) {
                     if (j < n_aff) {
                         const int j0 = j * kBN;
-                        tma_load_3d(sK, &p.tm_k0, 0, hk, j0, &ctl.kv_full[s]);
-                        tma_load_3d(sK + kRegion, &p.tm_k0, 64, hk, j0, &ctl.kv_full[s]);
-                        tma_load_3d(sV, &p.tm_v0, 0, hk, j0, &ctl.kv_full[s]);
-                        tma_load_3d(sV + kRegion, &p.tm_v0, 64, hk, j0, &ctl.kv_full[s]);
+                        tma_load_3d(dst_tile, tm_aff, 0, hk, j0, &full[s]);
+                        tma_load_3d(dst_tile + kRegion, tm_aff, 64, hk, j0, &full[s]);
                     } else {
                         const int r0 = (j - n_aff) * kBN;
-                        tma_load_4d(sK, &p.tm_k1, 0, hk, r0, b, &ctl.kv_full[s]);
-                        tma_load_4d(sK + kRegion, &p.tm_k1, 64, hk, r0, b, &ctl.kv_full[s]);
-                        tma_load_4d(sV, &p.tm_v1, 0, hk, r0, b, &ctl.kv_full[s]);
-                        tma_load_4d(sV + kRegion, &p.tm_v1, 64, hk, r0, b, &ctl.kv_full[s]);
+                        tma_load_4d(dst_tile, tm_own, 0, hk, r0, b, &full[s]);
+                        tma_load_4d(dst_tile + kRegion, tm_own, 64, hk, r0, b, &full[s]);
                     }
                 }
             }
         }
-    producers_done:;
-    } else if (warp == kMmaWarp) {
+    } else if (wg == 2) {
+        setmaxnreg_dec<kRegOther>();
+        if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
+        // Order per key tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).  tcgen05 MMAs of one
+        // thread run in issue order, so S_X(j+1) may overwrite the columns P_X(j) occupies,
+        // and the completion of S_X(j) implies that of PV_X(j-1).
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
             const uint32_t idO = idesc_bf16(kBM, kD, false, true);
-            auto issue_s = [&](int j) {
-                const uint32_t sK = base + kTileBytes * (1 + 2 * (j % kStages));
-                const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * kBN;
+            auto issue_s = [&](int t, int j) {
+                const uint32_t k_tile = sK(j % kKStages), q_tile = sQ(t);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
                     const uint32_t ko = (uint32_t)(k >> 2) * kRegion + (uint32_t)(k & 3) * 32u;
-                    umma_ss(d, sdesc_sw128(sQ + ko, 16, 1024), sdesc_sw128(sK + ko, 16, 1024), idS,
-                            k > 0);
+                    umma_ss(tmem + col_s(t), sdesc_sw128(q_tile + ko, 16, 1024),
+                            sdesc_sw128(k_tile + ko, 16, 1024), idS, k > 0);
                 }
-                umma_commit(&ctl.s_full[j & 1]);
+                umma_commit(&ctl.s_full[t]);
+            };
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t v_tile = sV(j % kVStages);
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k)
+                    umma_ts(tmem + col_o(t), tmem + col_s(t) + k * 8,
+                            sdesc_sw128(v_tile + k * 2048, kRegion, 1024), idO, (j > 0 || k > 0));
             };
             bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status) &&
-                      wait_bar(&ctl.kv_full[0], 0, abort_flag, dev_status);
+                      wait_bar(&ctl.k_full[0], 0, abort_flag, dev_status);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                for (int t = 0; t < n_qt; ++t) issue_s(t, 0);
+                umma_commit(&ctl.k_empty[0]);
             }
             for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) {
-                    ok = wait_bar(&ctl.kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
+                const bool more = j + 1 < n_kv;
+                ok = wait_bar(&ctl.v_full[j % kVStages], (j / kVStages) & 1, abort_flag, dev_status) &&
+                     wait_bar(&ctl.p_full[0], j & 1, abort_flag, dev_status);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(0, j);
+                if (more) {
+                    ok = wait_bar(&ctl.k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
                                   abort_flag, dev_status);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(j + 1);
+                    issue_s(0, j + 1);
                 }
-                ok = wait_bar(&ctl.p_full[j & 1], (j >> 1) & 1, abort_flag, dev_status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t sV = base + kTileBytes * (2 + 2 * (j % kStages));
-                const uint32_t p_tmem = tmem + kColS + (uint32_t)(j & 1) * kBN;
-#pragma unroll
-                for (int k = 0; k < kBN / 16; ++k)
-                    umma_ts(tmem + kColO, p_tmem + k * 8, sdesc_sw128(sV + k * 2048, kRegion, 1024),
-                            idO, (j > 0 || k > 0));
-                umma_commit(&ctl.o_done);
-                umma_commit(&ctl.kv_empty[j % kStages]);
+                if (n_qt > 1) {
+                    ok = wait_bar(&ctl.p_full[1], j & 1, abort_flag, dev_status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(1, j);
+                }
+                umma_commit(&ctl.v_empty[j % kVStages]);
+                if (more) {
+                    if (n_qt > 1) issue_s(1, j + 1);
+                    umma_commit(&ctl.k_empty[(j + 1) % kKStages]);
+                }
             }
             // no MMA may still run when TMEM is released
             umma_commit(&ctl.drain);
             mbar_wait(&ctl.drain, 0, kBudget);
         }
         __syncwarp();
+        }
     } else {
+        setmaxnreg_inc<kRegSoftmax>();
+        if (wg < n_qt) {
         // ------------------------------------------------------------------ softmax + epilogue
-        const int r = threadIdx.x;                         // query row in the tile
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int t = wg;                                  // Q tile of this warpgroup
+        const int r = threadIdx.x - t * 128;               // query row in the tile = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float c = p.scale_log2;                      // > 0
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            const int bs = j & 1;
-            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[bs], (j >> 1) & 1, abort_flag, dev_status));
+            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], j & 1, abort_flag, dev_status));
             if (!ok) break;
             tc_fence_after();
             uint32_t v[4][32];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_base + kColS + bs * kBN + cc * 32, v[cc]);
+            for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_base + col_s(t) + cc * 32, v[cc]);
             tmem_ld_wait();
             const int valid = tile_valid<kMode>(p, j);
             if (valid < kBN) {
@@ -346,54 +382,51 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 resc = true;
             }
             if (__any_sync(0xffffffffu, resc)) {
-                // O holds PV_0..PV_{j-1}: wait for the last one, rescale in place
-                ok = __all_sync(0xffffffffu, wait_bar(&ctl.o_done, (j - 1) & 1, abort_flag, dev_status));
-                if (!ok) break;
-                tc_fence_after();
+                // S_t(j) completed after PV_t(j-1): O_t is final up to tile j-1; rescale it
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + kColO + cc * 32, o);
+                    tmem_ld32(lane_base + col_o(t) + cc * 32, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(lane_base + kColO + cc * 32, o);
+                    tmem_st32(lane_base + col_o(t) + cc * 32, o);
                 }
                 tmem_st_wait();
             }
             const float neg_m = -m_used;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[2][32];
+            // P_j as bf16 pairs (64 columns) overwrites the first half of S_j's columns, 16
+            // columns at a time, so only one chunk of packed values is live
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     const float p0 = fast_exp2(fmaf(__uint_as_float(v[cc][i]), c, neg_m));
                     const float p1 = fast_exp2(fmaf(__uint_as_float(v[cc][i + 1]), c, neg_m));
                     ls[cc] += p0 + p1;
                     __nv_bfloat162 two = __floats2bfloat162_rn(p0, p1);   // low half = lower key
-                    pk[cc >> 1][(cc & 1) * 16 + (i >> 1)] = *reinterpret_cast<uint32_t*>(&two);
+                    pk[i >> 1] = *reinterpret_cast<uint32_t*>(&two);
                 }
+                tmem_st16(lane_base + col_s(t) + cc * 16, pk);
+            }
             l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-            // P_j (bf16 pairs, 64 columns) overwrites the first half of S_j's columns
-            tmem_st32(lane_base + kColS + bs * kBN, pk[0]);
-            tmem_st32(lane_base + kColS + bs * kBN + 32, pk[1]);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&ctl.p_full[bs]);
+            mbar_arrive(&ctl.p_full[t]);
         }
-        // `drain` is committed after the last PV; a parity wait on o_done could be fooled here,
-        // because PV_{n-2} may still be running when the last P is handed over
+        // `drain` is committed after the last PV of every tile
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain, 0, abort_flag, dev_status));
         if (ok) {
             tc_fence_after();
-            const int i = q0 + r;
+            const int i = q0 + t * kBM + r;
             const float inv_l = 1.f / l_sum;
             bf16* orow = p.out ? p.out + (((int64_t)b * p.n_rows + i) * p.Hq + h) * kD : nullptr;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(lane_base + kColO + cc * 32, o);
+                tmem_ld32(lane_base + col_o(t) + cc * 32, o);
                 tmem_ld_wait();
                 if (orow && i < p.n_rows) {
                     uint32_t pkd[16];
@@ -415,6 +448,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 p.stat_l[so] = l_sum;
             }
         }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -425,7 +459,9 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
 // ------------------------------------------------------------------------------------------
 // Second probe pass.
 constexpr int kCsStages = 2;
-constexpr int kCsThreads = (kProdWarp + 1) * 32;   // one producer warp
+constexpr int kCsMmaWarp = 4;
+constexpr int kCsProdWarp = 5;
+constexpr int kCsThreads = (kCsProdWarp + 1) * 32;   // one producer warp
 constexpr uint32_t kCsSmemBytes = kTileBytes * (1 + kCsStages) + 1024;
 constexpr uint32_t kCsTmemCols = 256;
 
@@ -485,7 +521,7 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
         ctl.abort = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kCsMmaWarp) {
         tmem_alloc(&ctl.tmem_base, kCsTmemCols);
         tmem_relinquish();
     }
@@ -494,7 +530,7 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
-    if (warp == kProdWarp) {
+    if (warp == kCsProdWarp) {
         const float* sm_row = p.stat_m + ((int64_t)b * p.Hq + h) * p.P;
         const float* sl_row = p.stat_l + ((int64_t)b * p.Hq + h) * p.P;
         const int32_t* mrow = p.masked + (int64_t)b * p.m;
@@ -542,7 +578,7 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
             tma_gather4(sB + kRegion + o, &p.tm_q, 64, rows[0], rows[1], rows[2], rows[3], &ctl.b_full[s]);
             if (lane != 0) mbar_arrive(&ctl.b_full[s]);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kCsMmaWarp) {
         if (lane == 0) {
             const uint32_t id = idesc_bf16(kBN, kBN, false, false);
             bool ok = wait_bar(&ctl.a_full, 0, abort_flag, dev_status);
@@ -599,7 +635,7 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
+    if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
 }
 
 // ---- host: tensor maps -----------------------------------------------------------------------
@@ -643,7 +679,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, i
 
 template <int kMode>
 int launch_attn(const AttnParams& prm, int B, cudaStream_t stream) {
-    const int64_t ctas = (int64_t)B * prm.Hq * ((prm.n_rows + kBM - 1) / kBM);
+    const int64_t ctas = (int64_t)B * prm.Hq * ((prm.n_rows + kQT * kBM - 1) / (kQT * kBM));
     if (ctas == 0) return ACACHE_OK;
     if (ctas > 0x7fffffff) return ACACHE_ERR_INVALID_ARG;
     auto kern = tc_attn_kernel<kMode>;
