@@ -57,7 +57,8 @@ constexpr int kQT = 2;                      // Q tiles per CTA: 256 query rows s
 constexpr int kBN = 128;                    // keys per tile
 constexpr int kKStages = 3;                 // K ring: a K tile is free once S_B has read it
 constexpr int kVStages = 2;                 // V ring: a V tile is free once PV_B has read it
-constexpr int kMmaWarp = 8;                 // warpgroup 2: TMEM allocation + the MMA thread
+constexpr int kMmaWarp = 8;                 // warpgroup 2: TMEM allocation; warps 8 and 9 each
+                                            // issue the MMAs of one Q tile
 constexpr int kProdWarp = 12;               // warpgroup 3: the 4 TMA producer warps
 constexpr int kProdWarps = 4;               // one per SM sub-partition: gather4 issue runs in
                                             // parallel on the four of them
@@ -103,7 +104,8 @@ struct AttnCtl {
     uint64_t v_empty[kVStages];
     uint64_t s_full[kQT];
     uint64_t p_full[kQT];
-    uint64_t drain;
+    uint64_t drain[kQT];
+    uint64_t turn[kQT];     // softmax ping-pong: turn[t] completes when tile t may exponentiate
     uint32_t tmem_base;
     int abort;
 };
@@ -163,19 +165,21 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 1);
+        // a K or V stage is free once the MMA thread of every present Q tile is done with it
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&ctl.k_full[s], 1);
-            mbar_init(&ctl.k_empty[s], 1);
+            mbar_init(&ctl.k_empty[s], n_qt);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&ctl.v_full[s], 1);
-            mbar_init(&ctl.v_empty[s], 1);
+            mbar_init(&ctl.v_empty[s], n_qt);
         }
         for (int t = 0; t < kQT; ++t) {
             mbar_init(&ctl.s_full[t], 1);
             mbar_init(&ctl.p_full[t], 128);
+            mbar_init(&ctl.drain[t], 1);
+            mbar_init(&ctl.turn[t], 128);
         }
-        mbar_init(&ctl.drain, 1);
         ctl.abort = 0;
         fence_mbar_init();
     }
@@ -273,70 +277,62 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         }
     } else if (wg == 2) {
         setmaxnreg_dec<kRegOther>();
-        if (warp == kMmaWarp) {
-        // ------------------------------------------------------------------ MMA issuer
-        // Order per key tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).  tcgen05 MMAs of one
-        // thread run in issue order, so S_X(j+1) may overwrite the columns P_X(j) occupies,
-        // and the completion of S_X(j) implies that of PV_X(j-1).
-        if (lane == 0) {
+        // ------------------------------------------------------------------ MMA issuers
+        // Warp 8 issues the MMAs of Q tile A, warp 9 those of tile B, so the two chains never
+        // wait on each other and their issue runs on two SM sub-partitions.  Per key tile j a
+        // thread issues PV_t(j) once P_t(j) is in TMEM, then S_t(j+1).  tcgen05 MMAs of one
+        // thread run in issue order, so S_t(j+1) may overwrite the columns P_t(j) occupies,
+        // and the completion of S_t(j) implies that of PV_t(j-1).
+        const int t = warp - kMmaWarp;
+        if (t < n_qt && lane == 0) {
             const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
             const uint32_t idO = idesc_bf16(kBM, kD, false, true);
-            auto issue_s = [&](int t, int j) {
-                const uint32_t k_tile = sK(j % kKStages), q_tile = sQ(t);
+            const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
+            const uint64_t dq = sdesc_sw128(sQ(t), 16, 1024);
+            // descriptor start addresses advance in 16-byte units: K step k of a K-major tile
+            // is 32 bytes into region k / 4; of the MN-major V tile, 16 rows (2048 bytes)
+            auto issue_s = [&](int j) {
+                const uint64_t dk = sdesc_sw128(sK(j % kKStages), 16, 1024);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t ko = (uint32_t)(k >> 2) * kRegion + (uint32_t)(k & 3) * 32u;
-                    umma_ss(tmem + col_s(t), sdesc_sw128(q_tile + ko, 16, 1024),
-                            sdesc_sw128(k_tile + ko, 16, 1024), idS, k > 0);
+                    const uint64_t ko = ((uint64_t)(k >> 2) * kRegion + (uint64_t)(k & 3) * 32u) >> 4;
+                    umma_ss(d_s, dq + ko, dk + ko, idS, k > 0);
                 }
                 umma_commit(&ctl.s_full[t]);
+                umma_commit(&ctl.k_empty[j % kKStages]);
             };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t v_tile = sV(j % kVStages);
+            auto issue_pv = [&](int j) {
+                const uint64_t dv = sdesc_sw128(sV(j % kVStages), kRegion, 1024);
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)
-                    umma_ts(tmem + col_o(t), tmem + col_s(t) + k * 8,
-                            sdesc_sw128(v_tile + k * 2048, kRegion, 1024), idO, (j > 0 || k > 0));
+                    umma_ts(d_o, d_s + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (j > 0 || k > 0));
+                umma_commit(&ctl.v_empty[j % kVStages]);
             };
             bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status) &&
                       wait_bar(&ctl.k_full[0], 0, abort_flag, dev_status);
             if (ok) {
                 tc_fence_after();
-                for (int t = 0; t < n_qt; ++t) issue_s(t, 0);
-                umma_commit(&ctl.k_empty[0]);
+                issue_s(0);
             }
             for (int j = 0; ok && j < n_kv; ++j) {
-                const bool more = j + 1 < n_kv;
                 ok = wait_bar(&ctl.v_full[j % kVStages], (j / kVStages) & 1, abort_flag, dev_status) &&
-                     wait_bar(&ctl.p_full[0], j & 1, abort_flag, dev_status);
+                     wait_bar(&ctl.p_full[t], j & 1, abort_flag, dev_status);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(0, j);
-                if (more) {
+                issue_pv(j);
+                if (j + 1 < n_kv) {
                     ok = wait_bar(&ctl.k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
                                   abort_flag, dev_status);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(0, j + 1);
-                }
-                if (n_qt > 1) {
-                    ok = wait_bar(&ctl.p_full[1], j & 1, abort_flag, dev_status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(1, j);
-                }
-                umma_commit(&ctl.v_empty[j % kVStages]);
-                if (more) {
-                    if (n_qt > 1) issue_s(1, j + 1);
-                    umma_commit(&ctl.k_empty[(j + 1) % kKStages]);
+                    issue_s(j + 1);
                 }
             }
             // no MMA may still run when TMEM is released
-            umma_commit(&ctl.drain);
-            mbar_wait(&ctl.drain, 0, kBudget);
+            umma_commit(&ctl.drain[t]);
+            mbar_wait(&ctl.drain[t], 0, kBudget);
         }
         __syncwarp();
-        }
     } else {
         setmaxnreg_inc<kRegSoftmax>();
         if (wg < n_qt) {
@@ -345,10 +341,17 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         const int r = threadIdx.x - t * 128;               // query row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float c = p.scale_log2;                      // > 0
+        // With two Q tiles the warpgroups take turns: A(0), B(0), A(1), B(1), ...  Each then
+        // has the SM's issue slots and exponential units to itself, and the tensor core runs
+        // one tile's MMAs while the other tile's softmax runs, instead of both at once.
+        const bool pingpong = n_qt > 1;
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], j & 1, abort_flag, dev_status));
+            if (ok && pingpong && (t == 1 || j > 0))
+                ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], (t == 0 ? j - 1 : j) & 1,
+                                                      abort_flag, dev_status));
             if (!ok) break;
             tc_fence_after();
             uint32_t v[4][32];
@@ -415,9 +418,10 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&ctl.p_full[t]);
+            if (pingpong) mbar_arrive(&ctl.turn[t ^ 1]);
         }
-        // `drain` is committed after the last PV of every tile
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain, 0, abort_flag, dev_status));
+        // drain[t] is committed after the last PV of this tile
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain[t], 0, abort_flag, dev_status));
         if (ok) {
             tc_fence_after();
             const int i = q0 + t * kBM + r;
