@@ -31,6 +31,13 @@ ACACHE_DEVFN float fast_exp2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (three-input form of max.f32 on sm_100 and later)
+ACACHE_DEVFN float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 ACACHE_DEVFN float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -103,7 +103,8 @@ struct AttnCtl {
     uint64_t v_full[kVStages];
     uint64_t v_empty[kVStages];
     uint64_t s_full[kQT];
-    uint64_t p_full[kQT];
+    uint64_t p_half[kQT];   // first half of P_t(j) (keys 0-63) is in TMEM
+    uint64_t p_full[kQT];   // all of P_t(j) is in TMEM
     uint64_t drain[kQT];
     uint64_t turn[kQT];     // softmax ping-pong: turn[t] completes when tile t may exponentiate
     uint32_t tmem_base;
@@ -151,10 +152,13 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     auto sQ = [&](int t) { return base + kTileBytes * (uint32_t)t; };
     auto sK = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + s); };
     auto sV = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + kKStages + s); };
-    const int n_qb = (p.n_rows + kQT * kBM - 1) / (kQT * kBM);
-    const int qb = blockIdx.x % n_qb;
-    const int h = (blockIdx.x / n_qb) % p.Hq;
-    const int b = blockIdx.x / (n_qb * p.Hq);
+    // CTA order: query block slowest, so the full 256-row blocks of every (request, head)
+    // start first and the ragged last blocks fill the final wave
+    const int n_bh = gridDim.x / ((p.n_rows + kQT * kBM - 1) / (kQT * kBM));   // B * Hq
+    const int bh = blockIdx.x % n_bh;
+    const int qb = blockIdx.x / n_bh;
+    const int h = bh % p.Hq;
+    const int b = bh / p.Hq;
     const int hk = h / (p.Hq / p.Hkv);
     const int q0 = qb * kQT * kBM;
     const int n_qt = min(kQT, (p.n_rows - q0 + kBM - 1) / kBM);   // Q tiles present (1 or 2)
@@ -176,6 +180,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         }
         for (int t = 0; t < kQT; ++t) {
             mbar_init(&ctl.s_full[t], 1);
+            mbar_init(&ctl.p_half[t], 128);
             mbar_init(&ctl.p_full[t], 128);
             mbar_init(&ctl.drain[t], 1);
             mbar_init(&ctl.turn[t], 128);
@@ -301,12 +306,13 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 umma_commit(&ctl.s_full[t]);
                 umma_commit(&ctl.k_empty[j % kKStages]);
             };
-            auto issue_pv = [&](int j) {
+            // PV_t(j) in two halves of the key tile: keys 0-63 (k steps 0-3) as soon as the
+            // softmax has published the first half of P, keys 64-127 once all of P is in
+            auto issue_pv_half = [&](int j, int h) {
                 const uint64_t dv = sdesc_sw128(sV(j % kVStages), kRegion, 1024);
 #pragma unroll
-                for (int k = 0; k < kBN / 16; ++k)
+                for (int k = 4 * h; k < 4 * h + 4; ++k)
                     umma_ts(d_o, d_s + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (j > 0 || k > 0));
-                umma_commit(&ctl.v_empty[j % kVStages]);
             };
             bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status) &&
                       wait_bar(&ctl.k_full[0], 0, abort_flag, dev_status);
@@ -316,10 +322,15 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 ok = wait_bar(&ctl.v_full[j % kVStages], (j / kVStages) & 1, abort_flag, dev_status) &&
-                     wait_bar(&ctl.p_full[t], j & 1, abort_flag, dev_status);
+                     wait_bar(&ctl.p_half[t], j & 1, abort_flag, dev_status);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(j);
+                issue_pv_half(j, 0);
+                ok = wait_bar(&ctl.p_full[t], j & 1, abort_flag, dev_status);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv_half(j, 1);
+                umma_commit(&ctl.v_empty[j % kVStages]);
                 if (j + 1 < n_kv) {
                     ok = wait_bar(&ctl.k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
                                   abort_flag, dev_status);
@@ -349,15 +360,19 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], j & 1, abort_flag, dev_status));
-            if (ok && pingpong && (t == 1 || j > 0))
-                ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], (t == 0 ? j - 1 : j) & 1,
-                                                      abort_flag, dev_status));
             if (!ok) break;
             tc_fence_after();
+            // S_t(j) is read into registers as soon as it is ready -- typically while the tensor
+            // core is idle -- before waiting for this warpgroup's turn: TMEM reads slow down
+            // concurrent MMAs, and the other tile's MMAs run during the other turn
             uint32_t v[4][32];
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_base + col_s(t) + cc * 32, v[cc]);
             tmem_ld_wait();
+            if (pingpong && (t == 1 || j > 0))
+                ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], (t == 0 ? j - 1 : j) & 1,
+                                                      abort_flag, dev_status));
+            if (!ok) break;
             const int valid = tile_valid<kMode>(p, j);
             if (valid < kBN) {
 #pragma unroll
@@ -366,15 +381,17 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     for (int i = 0; i < 32; ++i)
                         if (cc * 32 + i >= valid) v[cc][i] = __float_as_uint(-INFINITY);
             }
-            // row maximum of the raw logits (four independent chains)
+            // row maximum of the raw logits (four independent chains of three-input maxima)
             float mx[4];
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                mx[cc] = __uint_as_float(v[cc][0]);
+                mx[cc] = max3f(__uint_as_float(v[cc][0]), __uint_as_float(v[cc][1]), __uint_as_float(v[cc][2]));
 #pragma unroll
-                for (int i = 1; i < 32; ++i) mx[cc] = fmaxf(mx[cc], __uint_as_float(v[cc][i]));
+                for (int i = 3; i < 31; i += 2)
+                    mx[cc] = max3f(mx[cc], __uint_as_float(v[cc][i]), __uint_as_float(v[cc][i + 1]));
+                mx[cc] = fmaxf(mx[cc], __uint_as_float(v[cc][31]));
             }
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
+            const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
             float alpha = 1.f;
             bool resc = false;
             if (j == 0) {
@@ -400,7 +417,9 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             const float neg_m = -m_used;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
             // P_j as bf16 pairs (64 columns) overwrites the first half of S_j's columns, 16
-            // columns at a time, so only one chunk of packed values is live
+            // columns at a time, so only one chunk of packed values is live.  Keys 0-63 are
+            // published first (p_half) so the first half of PV_j runs while keys 64-127 are
+            // exponentiated.
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t pk[16];
@@ -413,6 +432,11 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     pk[i >> 1] = *reinterpret_cast<uint32_t*>(&two);
                 }
                 tmem_st16(lane_base + col_s(t) + cc * 16, pk);
+                if (cc == 1) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&ctl.p_half[t]);
+                }
             }
             l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
             tmem_st_wait();
