@@ -414,8 +414,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 }
                 tmem_st_wait();
             }
-            const float neg_m = -m_used;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_used, -m_used);
+            uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
             // P_j as bf16 pairs (64 columns) overwrites the first half of S_j's columns, 16
             // columns at a time, so only one chunk of packed values is live.  Keys 0-63 are
             // published first (p_half) so the first half of PV_j runs while keys 64-127 are
@@ -425,9 +425,12 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(v[cc][i]), c, neg_m));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(v[cc][i + 1]), c, neg_m));
-                    ls[cc] += p0 + p1;
+                    // exponent arguments of two keys with one packed FMA
+                    float x0, x1;
+                    f2unpack(f2fma(f2pack(__uint_as_float(v[cc][i]), __uint_as_float(v[cc][i + 1])), c2, nm2),
+                             x0, x1);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    ls2[(i >> 1) & 1] = f2add(ls2[(i >> 1) & 1], f2pack(p0, p1));
                     __nv_bfloat162 two = __floats2bfloat162_rn(p0, p1);   // low half = lower key
                     pk[i >> 1] = *reinterpret_cast<uint32_t*>(&two);
                 }
@@ -438,7 +441,10 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     mbar_arrive(&ctl.p_half[t]);
                 }
             }
-            l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            float l0, l1, l2, l3;
+            f2unpack(ls2[0], l0, l1);
+            f2unpack(ls2[1], l2, l3);
+            l_sum = l_sum * alpha + ((l0 + l1) + (l2 + l3));
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&ctl.p_full[t]);
