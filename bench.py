@@ -299,6 +299,17 @@ def dist_setup(args):
     return world, rank, local
 
 
+def reduce_max(x, device=None):
+    """Max of a per-rank float over the default process group (the timing reduction of the
+    multi-GPU replicas); the identity without a process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, w, world, rank):
     if rank != 0:
         return
@@ -326,6 +337,9 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, w, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -340,12 +354,7 @@ def main():
             dist.barrier()
 
     def max_over_ranks(x):
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([x], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return x
+        return reduce_max(x, dev)
 
     ev = {"select": [], "slot": []}
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv")
