@@ -210,9 +210,15 @@ int acache_slot_attention(const acache_attn_desc* desc, int batch, int n_q, cons
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return ACACHE_ERR_INVALID_ARG;
     cudaStream_t stream = (cudaStream_t)stream_;
-    if (tc_supported(a))
+    if (tc_supported(a)) {
+        // few query rows per KV head (the block-decode step): the kernel that packs a GQA
+        // group's heads into one K/V stream and splits the keys over a cluster
+        if (tc_decode_preferred(a, n_q))
+            return launch_tc_decode_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
+                                              num_slots, out, dev_status, stream);
         return launch_tc_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
                                         num_slots, out, dev_status, stream);
+    }
     return launch_simt_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
                                       num_slots, out, dev_status, stream);
 }

@@ -5,29 +5,26 @@
 // per-request read-slot map).  The page's prototype is a Triton kernel on A100; this is a
 // GB300-first design:
 //
-// tc_attn_kernel  (probe forward and read-slot attention; one CTA per 128 query rows of one
-//                  (request, query head); 256 threads, 1 CTA per SM)
-//   warps 0-3  softmax + epilogue: thread r owns query row r (= TMEM lane r)
-//   warp  4    TMEM allocation and the single MMA-issuing thread
-//   warps 5-7  TMA producers.  Read-slot keys: the 128 `tile::gather4` loads of a tile
-//              (4 rows x 64 columns of K or V each, rows resolved through the read-slot map)
-//              are spread over the 96 producer lanes, so the per-instruction issue cost is
-//              shared by 3 warps;
-//              probe keys: the affix rows and the request's own rows are contiguous per KV
-//              head, so warp 5 loads each tile with 4 tiled box loads.  All loads land in the
-//              128-byte-swizzled K-major layout tcgen05.mma reads and complete on the stage's
-//              mbarrier by byte count (warp 5 announces the bytes; a load that completes first
-//              leaves the count transiently negative, which the barrier allows).  Q is 2 tiled
-//              box loads.
-//   TMEM (512 columns): S double buffer [0,128) [128,256) (fp32), O [256,384) (fp32).
-//   Per key tile j:  S_j = Q K_j^T (SS MMA, M=N=128, K=128)  ->  softmax threads read S_j,
-//   exponentiate in base 2 against a lazily raised row maximum (the maximum only moves
-//   when it grows by more than 2^8, then O and the row sum are rescaled in place), and
-//   write P_j as packed bf16 back over S_j's columns  ->  O += P_j V_j (TS MMA, P from
-//   TMEM, V from shared memory as an MN-major operand).  S_{j+1} is issued before PV_j, so
-//   the tensor core works on the next tile while the softmax threads exponentiate.
-//   The kernel emits O / row sum and, for the probe, the row statistics (max, sum) that
-//   the second probe pass needs to normalise probabilities exactly.
+// tc_attn_kernel  (probe forward and read-slot attention at a recompute point; one CTA per
+//                  256 query rows -- two 128-row Q tiles A and B -- of one (request, query
+//                  head); 512 threads in four warpgroups, 1 CTA per SM)
+//   WG0, WG1  softmax + epilogue of tile A / B: thread r owns query row r (= TMEM lane r).
+//             Per key tile j: read S_t(j) from TMEM, row maximum, exponentiate in base 2
+//             against a lazily raised maximum (it only moves when it grows by more than 2^8;
+//             then O_t and the row sum are rescaled in TMEM), write P_t(j) as packed bf16 over
+//             S_t(j)'s first 64 columns, keys 0-63 published before keys 64-127.  The two
+//             warpgroups take turns (A(0), B(0), A(1), ...) so each has the SM's issue slots
+//             to itself while the tensor core works on the other tile.
+//   WG2       warp 8 allocates TMEM (S_A, S_B, O_A, O_B: 128 fp32 columns each); lane 0 of
+//             warp 8 issues tile A's MMAs, lane 0 of warp 9 tile B's:
+//             S_t(j) = Q_t K_j^T (SS, M = N = 128) and O_t += P_t(j) V_j (TS: P from TMEM,
+//             V an MN-major shared-memory operand), S_t(j+1) right after PV_t(j).
+//   WG3       TMA producers: warps 12-13 fill a 3-stage K ring, warps 14-15 a 2-stage V ring.
+//             Read-slot keys: each lane issues one `tile::gather4` per tile (4 pool rows x 64
+//             columns, rows resolved through the read-slot map one tile ahead).  Probe keys:
+//             the affix rows and the request's own rows are contiguous per KV head, so a tile
+//             is two tiled box loads.  Loads complete on the stage's mbarrier by byte count.
+//   setmaxnreg gives the softmax warpgroups 200 registers and WG2 / WG3 56.
 //
 // tc_colsum_kernel  (second probe pass: masked-to-affix attention mass; one CTA per
 //                    (request, query head, 128 affix keys))
@@ -670,45 +667,6 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     __syncthreads();
     tc_fence_after();
     if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
-}
-
-// ---- host: tensor maps -----------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-        else
-            (void)cudaGetLastError();
-    }
-    return fn;
-}
-
-// bf16 tensor of `rank` dims (innermost first, dims[0] = head_dim), 128-byte swizzle, box
-// {64, 1, ..., box_rows at dimension `row_dim`, 1, ...}; out-of-range elements read as zero.
-bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, int row_dim,
-              uint32_t box_rows) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t gdim[5], gstride[4];
-    cuuint32_t box[5], estr[5];
-    uint64_t stride = 2;
-    for (int i = 0; i < rank; ++i) {
-        gdim[i] = dims[i] ? dims[i] : 1;
-        if (i > 0) gstride[i - 1] = stride;
-        stride *= gdim[i];
-        box[i] = 1;
-        estr[i] = 1;
-    }
-    box[0] = 64;
-    box[row_dim] = box_rows;
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gdim, gstride, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int kMode>

@@ -1,9 +1,19 @@
 // tc_attn.cuh -- tensor-core (tcgen05 + TMEM) attention kernels for bf16, head_dim 128.
 #pragma once
 
+#include <cuda.h>
+
 #include "attn.cuh"
 
 namespace acache {
+
+// bf16 tensor of `rank` dims (innermost first, dims[0] = head_dim), contiguous, 128-byte
+// swizzle, box `box` (box[0] = 64: one 128-byte swizzle span); out-of-range elements read as
+// zero.  False when the driver entry point is missing or the encoding is rejected.
+bool make_map_box(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint32_t* box);
+// The same with box {64, 1, ..., box_rows at dimension row_dim, 1, ...}.
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, int row_dim,
+              uint32_t box_rows);
 
 // True when the tcgen05 kernels cover this geometry (bf16, head_dim 128).
 bool tc_supported(const AttnArgs& a);
@@ -12,6 +22,12 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
                              cudaStream_t stream);
+// Block-decode form of the read-slot attention (few query rows per KV head): true when it
+// streams fewer K/V tiles than the recompute-point kernel for this geometry.
+bool tc_decode_preferred(const AttnArgs& a, int n_q);
+int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
+                               const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                               int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream);
 int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                            const void* k_req, const void* v_req, const void* k_aff,
                            const void* v_aff, void* out, float* stat_m, float* stat_l,

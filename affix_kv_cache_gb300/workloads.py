@@ -248,6 +248,34 @@ def recompute_inputs(w: Workload, layer: int, point: int = 0, device="cpu") -> d
     return {"q_r": q_r.to(dt), "k_new": k_new.to(dt), "v_new": v_new.to(dt)}
 
 
+BLOCK = 32   # block length of the block-wise decode (Sec. 5, default settings)
+
+
+def decode_block_positions(w: Workload, step: int) -> list[int]:
+    """Logical positions of the block decoded at ``step``: the generation (mask) positions
+    are decoded left to right in blocks of ``BLOCK``, cycling when ``step`` passes the last."""
+    gen, pos = [], 0
+    for k, n in w.segments:
+        if k == SEG_MASK:
+            gen.extend(range(pos, pos + n))
+        pos += n
+    n_blocks = max(1, -(-len(gen) // BLOCK))
+    i = (step % n_blocks) * BLOCK
+    return gen[i:i + BLOCK]
+
+
+def decode_inputs(w: Workload, layer: int, step: int = 0, device="cpu") -> dict:
+    """One block-decode step of one layer: q_blk [B][n][Hq][d] the block's queries, k_blk /
+    v_blk [B][n][Hkv][d] its freshly computed K/V (n = the block's length)."""
+    n = len(decode_block_positions(w, step))
+    g = _gen(w, device, "decode", layer, step)
+    q = _randn((w.batch, n, w.hq, w.d), g, device)
+    k = _randn((w.batch, n, w.hkv, w.d), g, device)
+    v = _randn((w.batch, n, w.hkv, w.d), g, device)
+    dt = w.torch_dtype
+    return {"q_blk": q.to(dt), "k_blk": k.to(dt), "v_blk": v.to(dt)}
+
+
 def fresh_context(w: Workload, layer: int, device="cpu") -> dict:
     """Freshly recomputed K/V of every logical position of every request.
 

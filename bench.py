@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.CATALOGUE))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the block-decode measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle sample")
     ap.add_argument("--layers", type=int, default=0,
@@ -241,6 +242,88 @@ class Path:
         self.h_out.copy_(self.out[-1], non_blocking=True)
 
 
+class Decode:
+    """Block-decode steps on a Path's pools: per layer, the current block's fresh K/V are
+    written into the private slots of its positions, then its queries attend over all T
+    logical keys through the read map (one write + one slot attention launch per layer)."""
+
+    STEPS = 4   # distinct blocks cycled through
+
+    def __init__(self, path):
+        self.p = p = path
+        w = p.w
+        self.blocks = [wl.decode_block_positions(w, s) for s in range(self.STEPS)]
+        self.n = len(self.blocks[0])
+        self.inp = [[wl.decode_inputs(w, n, s, p.dev) for n in range(w.layers)] for s in range(self.STEPS)]
+        self.wslot = [p.read_slot[:, torch.tensor(b, device=p.dev)].contiguous() for b in self.blocks]
+        self.out = torch.empty_like(self.inp[0][0]["q_blk"])
+        # bytes a launch must move at least once: every distinct slot the batch reads (K and
+        # V), the queries, the output and the read map
+        distinct = int(torch.unique(p.read_slot).numel())
+        row = w.hkv * w.d * w.esize
+        qo = 2 * w.batch * self.n * w.hq * w.d * w.esize
+        self.unique_bytes = 2 * distinct * row + qo + w.batch * w.T * 4
+        self.logical_bytes = 2 * w.batch * w.T * row + qo + w.batch * w.T * 4
+        self.write_bytes = 2 * 2 * w.batch * self.n * row          # K and V, read + written
+
+    def run(self, step, kinds=("write", "attn")):
+        p, w, ac = self.p, self.p.w, self.p.ac
+        i = step % self.STEPS
+        for n in range(w.layers):
+            d = self.inp[i][n]
+            if "write" in kinds:
+                ac.acache_write_slots(p.desc, w.batch, self.n, self.wslot[i], d["k_blk"], d["v_blk"],
+                                      p.kc[n], p.vc[n], p.lay.num_slots, p.lay.private_begin)
+            if "attn" in kinds:
+                ac.acache_slot_attention(p.desc, w.batch, self.n, d["q_blk"], w.T, p.read_slot,
+                                         p.kc[n], p.vc[n], p.lay.num_slots, self.out)
+
+    def measure(self, reps, warmup, peaks):
+        """Times CUDA-graph replays of STEPS blocks x all layers: the decode loop is
+        launch-bound, so the launches are captured once and replayed without host work."""
+        for k in range(warmup):
+            self.run(k)
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        graphs = {}
+        for name, kinds in (("step", ("write", "attn")), ("attn", ("attn",)), ("write", ("write",))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(self.STEPS):
+                    self.run(i, kinds)
+            graphs[name] = g
+        torch.cuda.synchronize()
+        w = self.p.w
+        per = self.STEPS * w.layers          # launches of each kind per replay
+
+        def replay_ms(g):
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        t_step, t_attn, t_write = (replay_ms(graphs[k]) for k in ("step", "attn", "write"))
+        attn_ms, write_ms = t_attn / per, t_write / per
+        achieved = self.unique_bytes / (attn_ms / 1e3) / 1e9
+        return {
+            "workload": w.name, "block": self.n, "layers": w.layers, "replays": reps,
+            "timing": f"CUDA graph replay, {per} launches of each kind per replay",
+            "ms_per_layer": t_step / per, "attn_ms_per_launch": attn_ms, "write_ms_per_launch": write_ms,
+            "attn_tflops": 4.0 * self.n * w.T * w.d * w.hq * w.batch / (attn_ms / 1e3) / 1e12,
+            "logical_gather_gbs": self.logical_bytes / (attn_ms / 1e3) / 1e9,
+            "write_gbs": self.write_bytes / (write_ms / 1e3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "decode_slot_attention", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "peak_source": f"{peaks['source']} HBM copy",
+                         "bytes_per_launch": self.unique_bytes, "traffic": None},
+        }
+
+
 # ----------------------------------------------------------------------------- oracle
 def cpu_oracle_sample(w, budget_s):
     """Time the oracle as it stands on a bounded sample of the workload: request 0, layer by
@@ -399,6 +482,10 @@ def main():
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "ms_per_step": ems / n_e2e}
 
+    decode = None
+    if not args.no_decode:
+        decode = Decode(path).measure(max(args.steps, 5), 3, peaks)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         flops, secs, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
@@ -423,6 +510,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "slot_attention", "achieved": slot_achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": slot_achieved / peak,
                          "peak_source": f"{peaks['source']} bf16 sustained", "traffic": traffic},
+            "decode": decode,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": path.launches_per_step * args.steps,

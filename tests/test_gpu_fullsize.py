@@ -114,6 +114,54 @@ def test_fullsize_store_and_slot_attention(w):
         assert_out_close(got, ref[:, rows], "bf16", f"{w.name} slot attention request {b}")
 
 
+@pytest.mark.parametrize("w", FULL, ids=IDS)
+def test_fullsize_block_decode(w):
+    """One block-decode step over the whole batch: the block's fresh K/V are written into the
+    private slots of its positions, then its 32 queries attend over all T logical keys."""
+    lay = wl.slot_layout(w)
+    inp = wl.probe_inputs(w, 0, device="cuda")
+    rec = wl.recompute_inputs(w, 0, 0, device="cuda")
+    blk = wl.decode_inputs(w, 0, 3, device="cuda")
+    pos = wl.decode_block_positions(w, 3)
+    anchors = seeded_anchors(w)
+    d = desc_of(w)
+    st = status_tensor()
+    _, rs = oracle.build_slot_maps(anchors, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+    rsd = torch.from_numpy(rs).cuda()
+    kc = torch.zeros((lay.num_slots, w.hkv, w.d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ac.acache_write_slots(d, 1, w.L, lay.shared_slot.cuda(), inp["k_aff"], inp["v_aff"], kc, vc,
+                          lay.num_slots, 0, dev_status=st)
+    ac.acache_write_slots(d, w.batch, w.R, lay.private_slots.cuda(), rec["k_new"], rec["v_new"], kc, vc,
+                          lay.num_slots, lay.private_begin, dev_status=st)
+    wslot = rsd[:, pos].contiguous()
+    ac.acache_write_slots(d, w.batch, len(pos), wslot, blk["k_blk"], blk["v_blk"], kc, vc, lay.num_slots,
+                          lay.private_begin, dev_status=st)
+    out = torch.empty_like(blk["q_blk"])
+    ac.acache_slot_attention(d, w.batch, len(pos), blk["q_blk"], w.T, rsd, kc, vc, lay.num_slots, out,
+                             dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ws = wslot.long()
+    assert torch.equal(kc[ws], blk["k_blk"]) and torch.equal(vc[ws], blk["v_blk"])
+    # the first and last request against the oracle's own pool: shared affix + the request's
+    # fresh rows, with the block's rows overwritten in place
+    for b in (0, w.batch - 1):
+        pool_k = torch.cat([inp["k_aff"].cpu(), rec["k_new"][b].cpu()])
+        pool_v = torch.cat([inp["v_aff"].cpu(), rec["v_new"][b].cpu()])
+        _, rmap = oracle.build_slot_maps(anchors[b:b + 1], np.arange(w.L, dtype=np.int32),
+                                         (w.L + np.arange(w.R, dtype=np.int32))[None], T=w.T, l=w.l, L=w.L)
+        bslots = torch.from_numpy(rmap[0, pos].astype(np.int32))[None]
+        kb, vb, flags = oracle.write_slots(bslots, blk["k_blk"][b:b + 1].cpu(), blk["v_blk"][b:b + 1].cpu(),
+                                           pool_k, pool_v, private_begin=w.L)
+        assert flags == 0
+        pool_k = torch.from_numpy(kb).view(torch.bfloat16).reshape(pool_k.shape)
+        pool_v = torch.from_numpy(vb).view(torch.bfloat16).reshape(pool_v.shape)
+        ref = oracle.slot_attention(blk["q_blk"][b:b + 1].cpu(), rmap, pool_k, pool_v, scale=w.scale)
+        got = out[b:b + 1].float().cpu().numpy()
+        assert_out_close(got, ref, "bf16", f"{w.name} block decode request {b}")
+
+
 def test_fullsize_gather_matches_store():
     w = wl.LLADA_PAGED
     lay = wl.slot_layout(w)

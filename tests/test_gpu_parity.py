@@ -236,6 +236,64 @@ def test_slot_attention_parity(dtype, d, heads, n_q, T):
     assert_out_close(out.float().cpu().numpy(), ref, dtype, "slot attention")
 
 
+# Few query rows per KV head (the block-decode step): (B, n_q, Hq, Hkv, T).  The cases span
+# 4 / 2 / 1 replicas of the packed rows, key ranges split over clusters of 1, 2 and 4 CTAs,
+# GQA groups packed into one or two row blocks, and ragged last key tiles.
+DECODE_CASES = [
+    (2, 32, 4, 4, 1408),     # MHA block of 32: four replicas, clusters of 4
+    (1, 32, 2, 2, 4480),     # two units only: clusters of 4, 35 key tiles
+    (3, 5, 4, 4, 37),        # one ragged key tile
+    (2, 32, 8, 4, 300),      # g = 2: 64 packed rows, two replicas
+    (2, 32, 28, 4, 2624),    # g = 7: row blocks of 18 and 14 queries (126 + 98 rows)
+    (2, 100, 4, 4, 700),     # 100 rows: no replicas
+    (1, 1, 1, 1, 1),         # one query, one key
+    (2, 64, 4, 2, 129),      # g = 2, 128 packed rows, one key past a tile
+    (4, 32, 32, 32, 1408),   # the LLaDA-8B head geometry at T = 1408
+]
+
+
+@pytest.mark.parametrize("B,n_q,hq,hkv,T", DECODE_CASES)
+def test_decode_slot_attention_parity(B, n_q, hq, hkv, T):
+    d, num_slots = 128, 5000
+    g = torch.Generator().manual_seed(B * 1000 + n_q * 10 + hq + T)
+    kc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    q = (torch.randn((B, n_q, hq, d), generator=g) * 2).to(torch.bfloat16)
+    rs = torch.randint(0, num_slots, (B, T), generator=g, dtype=torch.int32)
+    scale = d ** -0.5
+    ref = oracle.slot_attention(q, rs, kc, vc, scale=scale)
+    out = torch.full((B, n_q, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = status_tensor()
+    ac.acache_slot_attention(ac.attn_desc(hq, hkv, d, scale, "bf16"), B, n_q, dev(q), T, dev(rs),
+                             dev(kc), dev(vc), num_slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(out.float().cpu().numpy(), ref, "bf16", "decode slot attention")
+
+
+def test_decode_slot_attention_peaked_rows():
+    """Rows whose maximum moves late (forces the in-TMEM rescale) and rows dominated by one
+    key: the replicas' and cluster ranks' partial maxima differ by large amounts."""
+    B, n_q, hq, hkv, T, d, num_slots = 1, 32, 4, 4, 2000, 128, 2500
+    g = torch.Generator().manual_seed(5)
+    kc = torch.randn((num_slots, hkv, d), generator=g)
+    vc = torch.randn((num_slots, hkv, d), generator=g)
+    q = torch.randn((B, n_q, hq, d), generator=g)
+    rs = torch.arange(T, dtype=torch.int32)[None].repeat(B, 1)
+    # key 1900 (last cluster rank, late tile) aligned with query 3; key 40 with query 7
+    kc[1900] = q[0, 3].reshape(hq, d)[:hkv] * 3
+    kc[40] = q[0, 7].reshape(hq, d)[:hkv] * 3
+    kc, vc, q = kc.to(torch.bfloat16), vc.to(torch.bfloat16), q.to(torch.bfloat16)
+    ref = oracle.slot_attention(q, rs, kc, vc, scale=d ** -0.5)
+    out = torch.empty((B, n_q, hq, d), dtype=torch.bfloat16, device="cuda")
+    st = status_tensor()
+    ac.acache_slot_attention(ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16"), B, n_q, dev(q), T, dev(rs),
+                             dev(kc), dev(vc), num_slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(out.float().cpu().numpy(), ref, "bf16", "peaked decode rows")
+
+
 def test_slot_attention_bad_slot_reads_zero_row():
     B, n_q, T, hq, hkv, d, num_slots = 1, 40, 150, 2, 2, 128, 300
     g = torch.Generator().manual_seed(11)
