@@ -6,7 +6,9 @@ Importing the package loads nothing; the library is loaded on first use and a mi
 library is an error.
 """
 from ._lib import (AcacheError, AttnDesc, attn_desc, acache_build_slot_maps,  # noqa: F401
-                   acache_gather_slots, acache_probe_scores, acache_probe_scores_noalloc,
+                   acache_gather_slots, acache_kv_deviation_scores, acache_probe_scores,
+                   acache_probe_scores_noalloc,
                    acache_probe_workspace_bytes,
-                   acache_slot_attention, acache_topk_anchors, acache_write_slots, lib,
+                   acache_slot_attention, acache_slot_attention_dropna, acache_topk_anchors,
+                   acache_write_slots, lib,
                    status_string, version)

@@ -24,11 +24,13 @@ ACACHE_ERR_WORKSPACE = -4
 ACACHE_ERR_TIMEOUT = -5
 ACACHE_F32 = 0
 ACACHE_BF16 = 1
+SLOT_NONE = -1
 DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
 
 EXPORTS = ("acache_status_string", "acache_version", "acache_probe_workspace_bytes",
            "acache_probe_scores", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
-           "acache_write_slots", "acache_slot_attention", "acache_gather_slots")
+           "acache_write_slots", "acache_slot_attention", "acache_gather_slots",
+           "acache_kv_deviation_scores", "acache_slot_attention_dropna")
 
 
 class AcacheError(RuntimeError):
@@ -75,6 +77,8 @@ def lib() -> ctypes.CDLL:
             "acache_write_slots": (I, [D, I, I, P, P, P, P, P, I64, I64, P, P]),
             "acache_slot_attention": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
             "acache_gather_slots": (I, [D, I, I, P, P, P, I64, P, P, P, P]),
+            "acache_kv_deviation_scores": (I, [D, I, I, P, P, P, P, P, P]),
+            "acache_slot_attention_dropna": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -180,3 +184,21 @@ def acache_gather_slots(desc, batch, seq_len, read_slot, k_cache, v_cache, num_s
                                    _p(v_cache), num_slots, _p(k_out), _p(v_out), _p(dev_status),
                                    _stream(stream))
     return _check("acache_gather_slots", st) if check else st
+
+
+def acache_kv_deviation_scores(desc, batch, affix_len, k_shared, v_shared, k_full, v_full, scores,
+                               stream=None, check=True):
+    """High-KV-deviation (CacheBlend-style) scores of one layer, accumulated into `scores`."""
+    st = lib().acache_kv_deviation_scores(ctypes.byref(desc), batch, affix_len, _p(k_shared),
+                                          _p(v_shared), _p(k_full), _p(v_full), _p(scores),
+                                          _stream(stream))
+    return _check("acache_kv_deviation_scores", st) if check else st
+
+
+def acache_slot_attention_dropna(desc, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
+                                 num_slots, out, dev_status=None, stream=None, check=True):
+    """Read-slot attention where read_slot entries equal to SLOT_NONE are discarded keys."""
+    st = lib().acache_slot_attention_dropna(ctypes.byref(desc), batch, n_q, _p(q), seq_len,
+                                            _p(read_slot), _p(k_cache), _p(v_cache), num_slots,
+                                            _p(out), _p(dev_status), _stream(stream))
+    return _check("acache_slot_attention_dropna", st) if check else st

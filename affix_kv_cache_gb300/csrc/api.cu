@@ -88,6 +88,35 @@ int launch_score_reduce(int B, int Hq, int L, const float* partial, float* score
 
 }  // namespace acache
 
+namespace acache {
+namespace {
+int slot_attention(const acache_attn_desc* desc, int batch, int n_q, const void* q, int seq_len,
+                   const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                   int64_t num_slots, void* out, int32_t* dev_status, void* stream_, bool drop_none) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (batch < 0 || n_q < 0 || seq_len < 0 || num_slots < 0) return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || n_q == 0) return ACACHE_OK;
+    if (seq_len == 0) return ACACHE_ERR_INVALID_ARG;       // a softmax over no keys
+    if (!q || !read_slot || !k_cache || !v_cache || !out) return ACACHE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return ACACHE_ERR_INVALID_ARG;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (tc_supported(a)) {
+        // few query rows per KV head (the block-decode step): the kernel that packs a GQA
+        // group's heads into one K/V stream and splits the keys over a cluster
+        if (tc_decode_preferred(a, n_q))
+            return launch_tc_decode_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
+                                              num_slots, out, dev_status, stream, drop_none);
+        return launch_tc_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
+                                        num_slots, out, dev_status, stream, drop_none);
+    }
+    return launch_simt_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
+                                      num_slots, out, dev_status, stream, drop_none);
+}
+}  // namespace
+}  // namespace acache
+
 using namespace acache;
 
 extern "C" {
@@ -164,6 +193,20 @@ int acache_topk_anchors(const float* scores, int batch, int affix_len, int k, in
     return launch_topk(scores, batch, affix_len, k, anchors, dev_status, (cudaStream_t)stream);
 }
 
+int acache_kv_deviation_scores(const acache_attn_desc* desc, int batch, int affix_len,
+                               const void* k_shared, const void* v_shared, const void* k_full,
+                               const void* v_full, float* scores, void* stream) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (batch < 0 || affix_len < 0) return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || affix_len == 0) return ACACHE_OK;
+    if (!k_shared || !v_shared || !k_full || !v_full || !scores) return ACACHE_ERR_INVALID_ARG;
+    if (!aligned16(k_shared) || !aligned16(v_shared) || !aligned16(k_full) || !aligned16(v_full))
+        return ACACHE_ERR_INVALID_ARG;
+    return launch_kv_deviation(a.dtype, batch, affix_len, a.hkv, a.d, k_shared, v_shared, k_full,
+                               v_full, scores, (cudaStream_t)stream);
+}
+
 int acache_build_slot_maps(int batch, int seq_len, int affix_begin, int affix_len, int k,
                            const int32_t* anchors, const int32_t* shared_slot,
                            const int32_t* private_slots, int32_t* write_pos, int32_t* read_slot,
@@ -197,30 +240,21 @@ int acache_write_slots(const acache_attn_desc* desc, int batch, int rows,
                               num_slots, private_begin, dev_status, (cudaStream_t)stream);
 }
 
+
 int acache_slot_attention(const acache_attn_desc* desc, int batch, int n_q, const void* q,
                           int seq_len, const int32_t* read_slot, const void* k_cache,
                           const void* v_cache, int64_t num_slots, void* out,
-                          int32_t* dev_status, void* stream_) {
-    AttnArgs a;
-    if (int rc = check_desc(desc, &a)) return rc;
-    if (batch < 0 || n_q < 0 || seq_len < 0 || num_slots < 0) return ACACHE_ERR_INVALID_ARG;
-    if (batch == 0 || n_q == 0) return ACACHE_OK;
-    if (seq_len == 0) return ACACHE_ERR_INVALID_ARG;       // a softmax over no keys
-    if (!q || !read_slot || !k_cache || !v_cache || !out) return ACACHE_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-        return ACACHE_ERR_INVALID_ARG;
-    cudaStream_t stream = (cudaStream_t)stream_;
-    if (tc_supported(a)) {
-        // few query rows per KV head (the block-decode step): the kernel that packs a GQA
-        // group's heads into one K/V stream and splits the keys over a cluster
-        if (tc_decode_preferred(a, n_q))
-            return launch_tc_decode_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
-                                              num_slots, out, dev_status, stream);
-        return launch_tc_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
-                                        num_slots, out, dev_status, stream);
-    }
-    return launch_simt_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
-                                      num_slots, out, dev_status, stream);
+                          int32_t* dev_status, void* stream) {
+    return slot_attention(desc, batch, n_q, q, seq_len, read_slot, k_cache, v_cache, num_slots, out,
+                          dev_status, stream, false);
+}
+
+int acache_slot_attention_dropna(const acache_attn_desc* desc, int batch, int n_q, const void* q,
+                                 int seq_len, const int32_t* read_slot, const void* k_cache,
+                                 const void* v_cache, int64_t num_slots, void* out,
+                                 int32_t* dev_status, void* stream) {
+    return slot_attention(desc, batch, n_q, q, seq_len, read_slot, k_cache, v_cache, num_slots, out,
+                          dev_status, stream, true);
 }
 
 int acache_gather_slots(const acache_attn_desc* desc, int batch, int seq_len,

@@ -12,7 +12,8 @@ struct AttnArgs {
 
 // Keys of the read-slot attention: logical key t of request b lives in physical slot
 // read_slot[b][t] of the layer's pool (Sec. 4.1, App. C.1).  An out-of-range slot reads
-// as a zero row and is flagged.
+// as a zero row and is flagged.  With drop_none, an entry equal to ACACHE_SLOT_NONE is a
+// discarded key (the DropNA ablation, Sec. 5.3): it takes no part in the softmax.
 template <typename T>
 struct SlotKeys {
     const T* k_cache;
@@ -22,6 +23,10 @@ struct SlotKeys {
     int T_len;
     int hkv;
     int d;
+    bool drop_none;
+    ACACHE_DEVFN bool dropped(int b, int t) const {
+        return drop_none && read_slot[(int64_t)b * T_len + t] == ACACHE_SLOT_NONE;
+    }
     ACACHE_DEVFN bool rows(int b, int t, int hk, const T*& kr, const T*& vr,
                            int32_t* dev_status) const {
         const int64_t s = read_slot[(int64_t)b * T_len + t];
@@ -57,6 +62,7 @@ struct ProbeKeys {
     const T* k_aff;
     const T* v_aff;
     int l, L, P, hkv, d;
+    ACACHE_DEVFN bool dropped(int, int) const { return false; }
     ACACHE_DEVFN bool rows(int b, int t, int hk, const T*& kr, const T*& vr, int32_t*) const {
         if (t >= l && t < l + L) {
             const int64_t off = ((int64_t)(t - l) * hkv + hk) * d;
@@ -88,7 +94,7 @@ struct ProbeKeys {
 int launch_simt_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
                                int64_t num_slots, void* out, int32_t* dev_status,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool drop_none = false);
 int launch_simt_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                              const void* k_req, const void* v_req, const void* k_aff,
                              const void* v_aff, void* out, float* stat_m, float* stat_l,
@@ -113,5 +119,7 @@ int launch_build_maps(int batch, int T, int l, int L, int K, const int32_t* anch
                       cudaStream_t stream);
 int launch_topk(const float* scores, int batch, int L, int K, int32_t* anchors,
                 int32_t* dev_status, cudaStream_t stream);
+int launch_kv_deviation(int dtype, int B, int L, int Hkv, int d, const void* k_sh, const void* v_sh,
+                        const void* k_full, const void* v_full, float* scores, cudaStream_t stream);
 
 }  // namespace acache

@@ -46,7 +46,7 @@ simt_attention_kernel(Keys keys, const T* __restrict__ q, T* __restrict__ out, i
     for (int t0 = 0; t0 < T_len; t0 += 32) {
         const int t = t0 + lane;
         float s = -INFINITY;
-        if (t < T_len) {
+        if (t < T_len && !keys.dropped(b, t)) {
             const T *kr, *vr;
             s = 0.f;
             if (keys.rows(b, t, hk, kr, vr, dev_status)) {
@@ -57,8 +57,10 @@ simt_attention_kernel(Keys keys, const T* __restrict__ q, T* __restrict__ out, i
             }
         }
         const float m_new = fmaxf(m, warp_max(s));
-        const float alpha = fast_exp2(m - m_new);        // m = -inf on the first chunk -> 0
-        const float p = fast_exp2(s - m_new);
+        // while every key so far was discarded (m_new = -inf) exponentiate against 0
+        const float m_ref = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = fast_exp2(m - m_ref);        // m = -inf on the first chunk -> 0
+        const float p = fast_exp2(s - m_ref);
         l = l * alpha + warp_sum(p);
 #pragma unroll
         for (int x = 0; x < kPer; ++x) acc[x] *= alpha;
@@ -66,13 +68,14 @@ simt_attention_kernel(Keys keys, const T* __restrict__ q, T* __restrict__ out, i
         for (int u = 0; u < nvalid; ++u) {
             const float pu = __shfl_sync(0xffffffffu, p, u);
             const T *kr, *vr;
-            if (!keys.rows(b, t0 + u, hk, kr, vr, nullptr)) continue;   // zero value row
+            if (keys.dropped(b, t0 + u) || !keys.rows(b, t0 + u, hk, kr, vr, nullptr))
+                continue;   // a discarded key or a zero value row
 #pragma unroll
             for (int x = 0; x < kPer; ++x) acc[x] = fmaf(pu, to_f32(vr[lane + 32 * x]), acc[x]);
         }
         m = m_new;
     }
-    const float inv_l = 1.f / l;
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;   // no key left: zeros
     if (out) {
 #pragma unroll
         for (int x = 0; x < kPer; ++x) out[qoff + lane + 32 * x] = from_f32<T>(acc[x] * inv_l);
@@ -148,9 +151,10 @@ int launch_simt(Keys keys, const void* q, void* out, int B, int n_rows, int Hq, 
 int launch_simt_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
                                int64_t num_slots, void* out, int32_t* dev_status,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool drop_none) {
     ACACHE_DISPATCH_TD(a.dtype, a.d, {
-        SlotKeys<T> keys{(const T*)k_cache, (const T*)v_cache, read_slot, num_slots, T_len, a.hkv, D};
+        SlotKeys<T> keys{(const T*)k_cache, (const T*)v_cache, read_slot, num_slots, T_len, a.hkv, D,
+                         drop_none};
         return launch_simt<T, D>(keys, q, out, B, n_q, a.hq, a.hkv, T_len, a.scale * kLog2e,
                                  nullptr, nullptr, dev_status, stream);
     });

@@ -139,7 +139,10 @@ ACACHE_DEVFN int tile_valid(const AttnParams& p, int j) {
     return j < n_aff ? min(kBN, p.L - j * kBN) : min(kBN, p.P - (j - n_aff) * kBN);
 }
 
-template <int kMode>
+// kDrop (read-slot keys only): a read-slot entry equal to ACACHE_SLOT_NONE marks a logical
+// position whose K/V was discarded (the page's DropNA ablation, Sec. 5.3): the key takes
+// no part in the softmax, and a row with no key left outputs zeros.
+template <int kMode, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t dsm[];
@@ -241,7 +244,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                         const int64_t slot = p.read_slot[(int64_t)b * p.T_len + t];
                         if (slot >= 0 && slot < p.num_slots)
                             rows[u] = (int)(slot * p.Hkv + hk);
-                        else if (!is_v && half == 0)
+                        else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
                             flag(dev_status, ACACHE_DEV_BAD_SLOT);
                     }
                 }
@@ -356,6 +359,17 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
+            // discarded keys of tile j: bit i of drop[cc] = key 32 cc + i (loaded before the
+            // wait for S_t(j), which hides the latency)
+            uint32_t drop[4] = {0u, 0u, 0u, 0u};
+            if constexpr (kDrop) {
+                const int32_t* rs = p.read_slot + (int64_t)b * p.T_len;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int tk = j * kBN + cc * 32 + (threadIdx.x & 31);
+                    drop[cc] = __ballot_sync(0xffffffffu, tk < p.T_len && rs[tk] == ACACHE_SLOT_NONE);
+                }
+            }
             ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], j & 1, abort_flag, dev_status));
             if (!ok) break;
             tc_fence_after();
@@ -377,6 +391,15 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (cc * 32 + i >= valid) v[cc][i] = __float_as_uint(-INFINITY);
+            }
+            if constexpr (kDrop) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    if (drop[cc]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if ((drop[cc] >> i) & 1u) v[cc][i] = __float_as_uint(-INFINITY);
+                    }
             }
             // row maximum of the raw logits (four independent chains of three-input maxima)
             float mx[4];
@@ -411,7 +434,9 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 }
                 tmem_st_wait();
             }
-            const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_used, -m_used);
+            // a row whose keys so far were all discarded exponentiates against 0 (every value is -inf)
+            const float ms = (kDrop && m_used == -INFINITY) ? 0.f : m_used;
+            const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-ms, -ms);
             uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
             // P_j as bf16 pairs (64 columns) overwrites the first half of S_j's columns, 16
             // columns at a time, so only one chunk of packed values is live.  Keys 0-63 are
@@ -452,7 +477,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         if (ok) {
             tc_fence_after();
             const int i = q0 + t * kBM + r;
-            const float inv_l = 1.f / l_sum;
+            const float inv_l = (kDrop && !(l_sum > 0.f)) ? 0.f : 1.f / l_sum;
             bf16* orow = p.out ? p.out + (((int64_t)b * p.n_rows + i) * p.Hq + h) * kD : nullptr;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -669,12 +694,12 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
 }
 
-template <int kMode>
+template <int kMode, bool kDrop = false>
 int launch_attn(const AttnParams& prm, int B, cudaStream_t stream) {
     const int64_t ctas = (int64_t)B * prm.Hq * ((prm.n_rows + kQT * kBM - 1) / (kQT * kBM));
     if (ctas == 0) return ACACHE_OK;
     if (ctas > 0x7fffffff) return ACACHE_ERR_INVALID_ARG;
-    auto kern = tc_attn_kernel<kMode>;
+    auto kern = tc_attn_kernel<kMode, kDrop>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
@@ -690,7 +715,7 @@ bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == k
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool drop_none) {
     if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
         return ACACHE_ERR_INVALID_ARG;
     AttnParams prm{};
@@ -710,7 +735,7 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     prm.Hkv = a.hkv;
     prm.T_len = T_len;
     prm.scale_log2 = a.scale * kLog2e;
-    return launch_attn<kSlotKeys>(prm, B, stream);
+    return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream) : launch_attn<kSlotKeys>(prm, B, stream);
 }
 
 int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,

@@ -18,16 +18,18 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, i
 // True when the tcgen05 kernels cover this geometry (bf16, head_dim 128).
 bool tc_supported(const AttnArgs& a);
 
+// drop_none: read-slot entries equal to ACACHE_SLOT_NONE are discarded keys (DropNA).
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool drop_none = false);
 // Block-decode form of the read-slot attention (few query rows per KV head): true when it
 // streams fewer K/V tiles than the recompute-point kernel for this geometry.
 bool tc_decode_preferred(const AttnArgs& a, int n_q);
 int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
-                               int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream);
+                               int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream,
+                               bool drop_none = false);
 int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                            const void* k_req, const void* v_req, const void* k_aff,
                            const void* v_aff, void* out, float* stat_m, float* stat_l,

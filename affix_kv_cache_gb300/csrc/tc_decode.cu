@@ -112,7 +112,9 @@ ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_f
 // lanes of a warp over the banks).
 ACACHE_DEVFN uint32_t part_off(int r, int q) { return (uint32_t)r * 512u + (uint32_t)((q ^ (r & 31)) << 4); }
 
-template <int REP>
+// kDrop: a read-slot entry equal to ACACHE_SLOT_NONE marks a discarded key (the page's
+// DropNA ablation, Sec. 5.3): it takes no part in the softmax.
+template <int REP, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_decode_kernel(const __grid_constant__ DecParams p) {
     extern __shared__ uint8_t dsm[];
@@ -203,7 +205,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
                     const int64_t slot = rs[t];
                     if (slot >= 0 && slot < p.num_slots)
                         rows[u] = (int)(slot * p.Hkv + hk);
-                    else if (!is_v && half == 0)
+                    else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
                         flag(dev_status, ACACHE_DEV_BAD_SLOT);
                 }
             }
@@ -294,6 +296,18 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
         float m_used = -INFINITY, l_sum = 0.f;
         for (int j = 0; j < n_kv; ++j) {
             const int sb = j & 1;
+            // discarded keys of this warp's key group: bit i of drop[cc] = key kb + 32 cc + i
+            uint32_t drop[NC];
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) drop[cc] = 0u;
+            if constexpr (kDrop) {
+                const int32_t* rs = p.read_slot + (int64_t)b * p.T_len;
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) {
+                    const int tk = (kt0 + j) * kBN + kb + cc * 32 + lane;
+                    drop[cc] = __ballot_sync(0xffffffffu, tk < p.T_len && rs[tk] == ACACHE_SLOT_NONE);
+                }
+            }
             ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[sb], (j >> 1) & 1, abort_flag, dev_status));
             if (!ok) break;
             tc_fence_after();
@@ -308,6 +322,15 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (cc * 32 + i >= valid) v[cc][i] = __float_as_uint(-INFINITY);
+            }
+            if constexpr (kDrop) {
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc)
+                    if (drop[cc]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if ((drop[cc] >> i) & 1u) v[cc][i] = __float_as_uint(-INFINITY);
+                    }
             }
             float mx[NC];
 #pragma unroll
@@ -516,16 +539,16 @@ bool decode_geom(int B, int n_q, int g, int hkv, int T_len, DecodeGeom& dg) {
     return true;
 }
 
-// Per device and replication: 0 = not prepared yet, 1 = ready, otherwise the status to return.
-// Preparing twice is harmless, so a race between threads only repeats the work.
-std::atomic<int> g_prepared[3][64];
+// Per device and kernel variant: 0 = not prepared yet, 1 = ready, otherwise the status to
+// return.  Preparing twice is harmless, so a race between threads only repeats the work.
+std::atomic<int> g_prepared[6][64];
 
-template <int REP>
+template <int REP, bool kDrop>
 int prepare(int dev) {
-    std::atomic<int>& st = g_prepared[REP == 4 ? 2 : REP - 1][dev];
+    std::atomic<int>& st = g_prepared[(REP == 4 ? 2 : REP - 1) * 2 + (kDrop ? 1 : 0)][dev];
     const int known = st.load(std::memory_order_acquire);
     if (known) return known == 1 ? ACACHE_OK : known;
-    auto kern = tc_decode_kernel<REP>;
+    auto kern = tc_decode_kernel<REP, kDrop>;
     int rc = ACACHE_OK;
     cudaFuncAttributes fa;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
@@ -539,15 +562,15 @@ int prepare(int dev) {
     return rc;
 }
 
-template <int REP>
+template <int REP, bool kDrop>
 int launch_rep(const DecParams& prm, int64_t ctas, cudaStream_t stream) {
-    auto kern = tc_decode_kernel<REP>;
+    auto kern = tc_decode_kernel<REP, kDrop>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
     }
-    if (int rc = prepare<REP>(dev)) return rc;
+    if (int rc = prepare<REP, kDrop>(dev)) return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kThreads);
@@ -584,7 +607,8 @@ bool tc_decode_preferred(const AttnArgs& a, int n_q) {
 
 int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
-                               int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream) {
+                               int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream,
+                               bool drop_none) {
     if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
         return ACACHE_ERR_INVALID_ARG;
     const int g = a.hq / a.hkv;
@@ -613,10 +637,17 @@ int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q,
     prm.n_rb = dg.n_rb;
     prm.cs = dg.cs;
     prm.scale_log2 = a.scale * kLog2e;
+    if (drop_none) {
+        switch (dg.rep) {
+            case 4: return launch_rep<4, true>(prm, ctas, stream);
+            case 2: return launch_rep<2, true>(prm, ctas, stream);
+            default: return launch_rep<1, true>(prm, ctas, stream);
+        }
+    }
     switch (dg.rep) {
-        case 4: return launch_rep<4>(prm, ctas, stream);
-        case 2: return launch_rep<2>(prm, ctas, stream);
-        default: return launch_rep<1>(prm, ctas, stream);
+        case 4: return launch_rep<4, false>(prm, ctas, stream);
+        case 2: return launch_rep<2, false>(prm, ctas, stream);
+        default: return launch_rep<1, false>(prm, ctas, stream);
     }
 }
 

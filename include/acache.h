@@ -68,6 +68,11 @@ enum {
     ACACHE_DEV_TIMEOUT = 32       /* a bounded wait inside a kernel gave up                */
 };
 
+/* Read-slot map entry of a logical position whose K/V was discarded (the page's DropNA
+ * ablation, Sec. 5.3).  Only acache_slot_attention_dropna gives it that meaning; for every
+ * other call it is an out-of-range slot like any other negative value. */
+#define ACACHE_SLOT_NONE (-1)
+
 /* Attention geometry shared by the attention calls. */
 typedef struct {
     int32_t num_q_heads;    /* Hq                                                    */
@@ -149,6 +154,25 @@ ACACHE_API int acache_topk_anchors(const float* scores, int batch, int affix_len
                         int32_t* anchors, int32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * Alternative selector: high KV deviation (CacheBlend-style), ONE layer.
+ * Page: App. B.5 -- the variant keeps ACache's generation path and cache layout but ranks
+ * affix tokens by the difference between the affix-only KV cache and the full-prompt KV
+ * cache instead of by masked-to-affix attention.  Per request b and affix offset j:
+ *   scores[b][j] += sum over KV heads hk (ascending) of
+ *                   ||k_full[b][j][hk] - k_shared[j][hk]||_2 + ||v_full[b][j][hk] - v_shared[j][hk]||_2
+ * (float32 sums of squares with a fixed reduction order: bit-reproducible).  Zero `scores`
+ * before layer 0 and call the layers in order on one stream, then rank with
+ * acache_topk_anchors exactly as for the probe's scores.
+ *   k_shared, v_shared [L][Hkv][d]     the shared (affix-only) cache of the layer
+ *   k_full, v_full     [B][L][Hkv][d]  the affix tokens' K/V computed inside each request
+ *   scores             [B][L] float    ACCUMULATED in place
+ * Pointers must be 16-byte aligned.  No device-side errors are possible.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_kv_deviation_scores(const acache_attn_desc* a, int batch, int affix_len,
+                        const void* k_shared, const void* v_shared, const void* k_full,
+                        const void* v_full, float* scores, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Admission-time maps.  Page: Sec. 4.1-4.2 (write-side recomputation map and per-request
  * read-slot map, recorded once at admission).
  * The R = K + P recomputed logical positions are the anchor positions l + A_b and every
@@ -192,6 +216,21 @@ ACACHE_API int acache_write_slots(const acache_attn_desc* a, int batch, int rows
 ACACHE_API int acache_slot_attention(const acache_attn_desc* a, int batch, int n_q, const void* q,
                           int seq_len, const int32_t* read_slot, const void* k_cache,
                           const void* v_cache, int64_t num_slots, void* out,
+                          int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * (4b') Read-slot attention with discarded keys -- the DropNA ablation.  Page: Sec. 5.3
+ * (Figure 5) and App. B.4: the same anchors are recomputed, but every non-anchor affix
+ * entry of the cache is discarded instead of read from the shared region.
+ * Same arguments, layouts and errors as acache_slot_attention, except that a read-slot
+ * entry equal to ACACHE_SLOT_NONE marks a logical position without K/V: that key takes no
+ * part in the softmax (it is not a zero row) and raises no flag.  A query row whose keys
+ * are all discarded outputs zeros.  A DropNA map is what acache_build_slot_maps writes when
+ * every shared_slot entry is ACACHE_SLOT_NONE.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_slot_attention_dropna(const acache_attn_desc* a, int batch, int n_q,
+                          const void* q, int seq_len, const int32_t* read_slot,
+                          const void* k_cache, const void* v_cache, int64_t num_slots, void* out,
                           int32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------

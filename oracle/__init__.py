@@ -56,11 +56,13 @@ def _load():
             lib.ref_build_slot_maps.argtypes = [I, I, I, I, I, P, P, P, P, P]
             lib.ref_write_slots.argtypes = [I, I, I, I, I, P, P, P, P, P, L, L]
             lib.ref_gather_slots.argtypes = [I, I, I, I, I, P, P, P, L, P, P]
-            lib.ref_slot_attention.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P, L, P, I, P]
+            lib.ref_slot_attention.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P, L, P, I, I, P]
             lib.ref_dense_attention.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P]
+            lib.ref_kv_deviation.argtypes = [I, I, I, I, I, P, P, P, P, P]
             lib.ref_set_threads.argtypes = [I]
             for f in ("ref_probe_layer", "ref_topk", "ref_build_slot_maps", "ref_write_slots",
                       "ref_gather_slots", "ref_slot_attention", "ref_dense_attention",
+                      "ref_kv_deviation",
                       "ref_version", "ref_get_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -200,7 +202,9 @@ def gather_slots(read_slot, k_cache, v_cache):
     return ko, vo, flags
 
 
-def slot_attention(q, read_slot, k_cache, v_cache, *, scale, rows=None):
+def slot_attention(q, read_slot, k_cache, v_cache, *, scale, rows=None, drop_none=False):
+    """Read-slot attention (Sec. 4.3); with drop_none, read_slot entries of -1 are discarded
+    keys (DropNA, reading R7).  Returns float64 [B][nq][Hq][d]."""
     qa, dt = _raw(q)
     ka, _ = _raw(k_cache)
     va, _ = _raw(v_cache)
@@ -212,7 +216,7 @@ def slot_attention(q, read_slot, k_cache, v_cache, *, scale, rows=None):
     out = np.zeros((B, nq, Hq, d), np.float64)
     rc = _load().ref_slot_attention(B, nq, T, Hq, Hkv, d, float(scale), dt, _p(qa), _p(rs),
                                     _p(ka), _p(va), num_slots, _p(rw),
-                                    0 if rw is None else rw.shape[0], _p(out))
+                                    0 if rw is None else rw.shape[0], int(drop_none), _p(out))
     if rc != 0:
         raise ValueError("ref_slot_attention rejected its arguments")
     return out
@@ -230,3 +234,20 @@ def dense_attention(q, k, v, *, scale):
     if rc != 0:
         raise ValueError("ref_dense_attention rejected its arguments")
     return out
+
+
+def kv_deviation(k_shared, v_shared, k_full, v_full, scores=None):
+    """App. B.5 high-KV-deviation scores of one layer (reading R6), float64 [B][L]; added onto
+    ``scores`` if given.  k_shared/v_shared [L][Hkv][d]; k_full/v_full [B][L][Hkv][d]."""
+    ks, dt = _raw(k_shared)
+    vs, _ = _raw(v_shared)
+    kf, dt2 = _raw(k_full)
+    vf, _ = _raw(v_full)
+    assert dt == dt2
+    B, L, Hkv, d = kf.shape
+    assert ks.shape == (L, Hkv, d)
+    sc = np.zeros((B, L), np.float64) if scores is None else np.ascontiguousarray(scores, np.float64).copy()
+    rc = _load().ref_kv_deviation(B, L, Hkv, d, dt, _p(ks), _p(vs), _p(kf), _p(vf), _p(sc))
+    if rc != 0:
+        raise ValueError("ref_kv_deviation rejected its arguments")
+    return sc

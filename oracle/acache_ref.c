@@ -26,6 +26,13 @@
  *   R4  Ties in Top-K go to the lower affix offset; anchors are emitted ascending.
  *   R5  Recomputed rows are ordered by ascending logical position (anchors interleaved
  *       with the request's own rows); the i-th one is written to private slot i.
+ *   R6  The CacheBlend-style selector of App. B.5 ranks affix tokens by how far their K/V
+ *       inside the full prompt moved from the affix-only cache; the measure taken is the
+ *       L2 norm of the key difference plus that of the value difference, per KV head,
+ *       summed over KV heads and layers.
+ *   R7  DropNA (Sec. 5.3) throws away the cached K/V of every non-anchor affix position:
+ *       such a position has no key at all -- it is left out of the softmax, not read as a
+ *       zero row; a row left with no key outputs zeros.
  */
 #include <math.h>
 #include <stdint.h>
@@ -300,15 +307,16 @@ int ref_gather_slots(int B, int T, int Hkv, int d, int esize, const int32_t* rea
  * bidirectionally, over all T logical keys K_log[t] = k_cache[read_slot[b][t]].
  *   q   [B][nq][Hq][d], caches [num_slots][Hkv][d], out [B][nq][Hq][d] (double)
  *   rows [n_rows] or NULL: query rows to evaluate (same subset for every request)
+ *   drop_none: an entry equal to -1 is a discarded logical position (reading R7)
  * Returns 0, or -1 for a slot out of range.
  */
 int ref_slot_attention(int B, int nq, int T, int Hq, int Hkv, int d, double scale, int dtype,
                        const void* q, const int32_t* read_slot, const void* k_cache,
                        const void* v_cache, int64_t num_slots, const int32_t* rows, int n_rows,
-                       double* out) {
+                       int drop_none, double* out) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
     for (int64_t x = 0; x < (int64_t)B * T; ++x)
-        if (read_slot[x] < 0 || read_slot[x] >= num_slots) return -1;
+        if ((read_slot[x] < 0 || read_slot[x] >= num_slots) && !(drop_none && read_slot[x] == -1)) return -1;
     const int g = Hq / Hkv;
     if (!rows) n_rows = nq;
     const int64_t nitems = (int64_t)B * Hq;
@@ -320,17 +328,22 @@ int ref_slot_attention(int B, int nq, int T, int Hq, int Hkv, int d, double scal
             const int i = rows ? rows[ri] : ri;
             const int64_t qoff = (((int64_t)b * nq + i) * Hq + h) * d;
             double mx = -INFINITY;
+            int kept = 0;
             for (int t = 0; t < T; ++t) {
                 const int64_t slot = read_slot[(int64_t)b * T + t];
+                if (slot < 0) continue;                       /* discarded (R7) */
                 s[t] = scale * dot_row(q, qoff, k_cache, (slot * Hkv + hk) * d, d, dtype);
                 mx = s[t] > mx ? s[t] : mx;
+                ++kept;
             }
             double sum = 0.0;
-            for (int t = 0; t < T; ++t) sum += exp(s[t] - mx);
+            for (int t = 0; t < T; ++t)
+                if (read_slot[(int64_t)b * T + t] >= 0) sum += exp(s[t] - mx);
             double* o = out + qoff;
             for (int c = 0; c < d; ++c) o[c] = 0.0;
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; kept > 0 && t < T; ++t) {
                 const int64_t slot = read_slot[(int64_t)b * T + t];
+                if (slot < 0) continue;
                 const double pt = exp(s[t] - mx) / sum;
                 for (int c = 0; c < d; ++c) o[c] += pt * widen(v_cache, dtype, (slot * Hkv + hk) * d + c);
             }
@@ -372,5 +385,34 @@ int ref_dense_attention(int B, int nq, int T, int Hq, int Hkv, int d, double sca
         }
         free(w);
     }
+    return 0;
+}
+
+/*
+ * High-KV-deviation selector of one layer (App. B.5, reading R6): for every request b and
+ * affix offset j,
+ *   scores[b][j] += sum_hk ( ||k_full[b][j][hk] - k_sh[j][hk]|| + ||v_full[b][j][hk] - v_sh[j][hk]|| )
+ *   k_sh, v_sh [L][Hkv][d]; k_full, v_full [B][L][Hkv][d]; scores [B][L] (double, accumulated)
+ */
+int ref_kv_deviation(int B, int L, int Hkv, int d, int dtype, const void* k_sh, const void* v_sh,
+                     const void* k_full, const void* v_full, double* scores) {
+    if (B < 0 || L < 0 || Hkv <= 0 || d <= 0) return -1;
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < L; ++j) {
+            double dev = 0.0;
+            for (int hk = 0; hk < Hkv; ++hk) {
+                const int64_t so = ((int64_t)j * Hkv + hk) * d;
+                const int64_t fo = (((int64_t)b * L + j) * Hkv + hk) * d;
+                double sk = 0.0, sv = 0.0;
+                for (int c = 0; c < d; ++c) {
+                    const double dk = widen(k_full, dtype, fo + c) - widen(k_sh, dtype, so + c);
+                    const double dv = widen(v_full, dtype, fo + c) - widen(v_sh, dtype, so + c);
+                    sk += dk * dk;
+                    sv += dv * dv;
+                }
+                dev += sqrt(sk) + sqrt(sv);
+            }
+            scores[(int64_t)b * L + j] += dev;
+        }
     return 0;
 }
