@@ -9,6 +9,7 @@ from ._lib import (AcacheError, AttnDesc, attn_desc, acache_build_slot_maps,  # 
                    acache_gather_slots, acache_kv_deviation_scores, acache_probe_scores,
                    acache_probe_scores_noalloc,
                    acache_probe_workspace_bytes,
-                   acache_slot_attention, acache_slot_attention_dropna, acache_topk_anchors,
+                   acache_slot_attention, acache_slot_attention_dropna, acache_slot_attention_varlen,
+                   acache_store_attend, acache_topk_anchors,
                    acache_write_slots, lib,
                    status_string, version)

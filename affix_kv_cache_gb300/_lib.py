@@ -26,11 +26,13 @@ ACACHE_F32 = 0
 ACACHE_BF16 = 1
 SLOT_NONE = -1
 DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
+DEV_BAD_LENGTH = 64
 
 EXPORTS = ("acache_status_string", "acache_version", "acache_probe_workspace_bytes",
            "acache_probe_scores", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
            "acache_write_slots", "acache_slot_attention", "acache_gather_slots",
-           "acache_kv_deviation_scores", "acache_slot_attention_dropna")
+           "acache_kv_deviation_scores", "acache_slot_attention_dropna", "acache_slot_attention_varlen",
+           "acache_store_attend")
 
 
 class AcacheError(RuntimeError):
@@ -79,6 +81,8 @@ def lib() -> ctypes.CDLL:
             "acache_gather_slots": (I, [D, I, I, P, P, P, I64, P, P, P, P]),
             "acache_kv_deviation_scores": (I, [D, I, I, P, P, P, P, P, P]),
             "acache_slot_attention_dropna": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
+            "acache_slot_attention_varlen": (I, [D, I, P, I, I, P, P, I, P, P, P, I64, P, I, P, P]),
+            "acache_store_attend": (I, [D, I, I, P, P, P, P, P, I64, I64, I, P, I, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -202,3 +206,25 @@ def acache_slot_attention_dropna(desc, batch, n_q, q, seq_len, read_slot, k_cach
                                             _p(read_slot), _p(k_cache), _p(v_cache), num_slots,
                                             _p(out), _p(dev_status), _stream(stream))
     return _check("acache_slot_attention_dropna", st) if check else st
+
+
+def acache_slot_attention_varlen(desc, batch, q_start, max_q_rows, total_q_rows, q, kv_start,
+                                 max_seq_len, read_slot, k_cache, v_cache, num_slots, out,
+                                 drop_none=False, dev_status=None, stream=None, check=True):
+    """Read-slot attention over a ragged batch: q_start / kv_start are [B+1] int32 device
+    offsets into the flattened query rows and read-slot entries."""
+    st = lib().acache_slot_attention_varlen(ctypes.byref(desc), batch, _p(q_start), max_q_rows,
+                                            total_q_rows, _p(q), _p(kv_start), max_seq_len,
+                                            _p(read_slot), _p(k_cache), _p(v_cache), num_slots, _p(out),
+                                            int(bool(drop_none)), _p(dev_status), _stream(stream))
+    return _check("acache_slot_attention_varlen", st) if check else st
+
+
+def acache_store_attend(desc, batch, rows, write_slot, k_new, v_new, k_cache, v_cache, num_slots,
+                        private_begin, n_q, q, seq_len, read_slot, out, dev_status=None, stream=None,
+                        check=True):
+    """Store step then read-slot attention of one layer in one call (see include/acache.h)."""
+    st = lib().acache_store_attend(ctypes.byref(desc), batch, rows, _p(write_slot), _p(k_new), _p(v_new),
+                                   _p(k_cache), _p(v_cache), num_slots, private_begin, n_q, _p(q),
+                                   seq_len, _p(read_slot), _p(out), _p(dev_status), _stream(stream))
+    return _check("acache_store_attend", st) if check else st

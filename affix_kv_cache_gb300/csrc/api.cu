@@ -92,7 +92,8 @@ namespace acache {
 namespace {
 int slot_attention(const acache_attn_desc* desc, int batch, int n_q, const void* q, int seq_len,
                    const int32_t* read_slot, const void* k_cache, const void* v_cache,
-                   int64_t num_slots, void* out, int32_t* dev_status, void* stream_, bool drop_none) {
+                   int64_t num_slots, void* out, int32_t* dev_status, void* stream_, bool drop_none,
+                   bool after_store = false) {
     AttnArgs a;
     if (int rc = check_desc(desc, &a)) return rc;
     if (batch < 0 || n_q < 0 || seq_len < 0 || num_slots < 0) return ACACHE_ERR_INVALID_ARG;
@@ -107,9 +108,9 @@ int slot_attention(const acache_attn_desc* desc, int batch, int n_q, const void*
         // group's heads into one K/V stream and splits the keys over a cluster
         if (tc_decode_preferred(a, n_q))
             return launch_tc_decode_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
-                                              num_slots, out, dev_status, stream, drop_none);
+                                              num_slots, out, dev_status, stream, drop_none, after_store);
         return launch_tc_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
-                                        num_slots, out, dev_status, stream, drop_none);
+                                        num_slots, out, dev_status, stream, drop_none, after_store);
     }
     return launch_simt_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
                                       num_slots, out, dev_status, stream, drop_none);
@@ -223,6 +224,37 @@ int acache_build_slot_maps(int batch, int seq_len, int affix_begin, int affix_le
                              read_slot, dev_status, (cudaStream_t)stream);
 }
 
+int acache_store_attend(const acache_attn_desc* desc, int batch, int rows, const int32_t* write_slot,
+                        const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                        int64_t num_slots, int64_t private_begin, int n_q, const void* q, int seq_len,
+                        const int32_t* read_slot, void* out, int32_t* dev_status, void* stream) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    // validate both halves before launching either
+    if (batch < 0 || rows < 0 || n_q < 0 || seq_len < 0 || num_slots < 0 || private_begin < 0 ||
+        private_begin > num_slots)
+        return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0) return ACACHE_OK;
+    const bool store = rows > 0, attend = n_q > 0;
+    if (store && (!write_slot || !k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return ACACHE_ERR_INVALID_ARG;
+    if (attend && (seq_len == 0 || !q || !read_slot || !out || !aligned16(q) || !aligned16(out)))
+        return ACACHE_ERR_INVALID_ARG;
+    if ((store || attend) && (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)))
+        return ACACHE_ERR_INVALID_ARG;
+    if (store) {
+        const int64_t row_bytes = (int64_t)a.hkv * a.d * elem_bytes(a.dtype);
+        if (int rc = launch_write_slots(batch, rows, write_slot, k_new, v_new, k_cache, v_cache, row_bytes,
+                                        num_slots, private_begin, dev_status, (cudaStream_t)stream))
+            return rc;
+    }
+    if (!attend) return ACACHE_OK;
+    // the tensor-core attention starts its prologue while the store drains (programmatic
+    // dependent launch); its producers wait for the store before reading the pool
+    return slot_attention(desc, batch, n_q, q, seq_len, read_slot, k_cache, v_cache, num_slots, out,
+                          dev_status, stream, false, store && tc_supported(a));
+}
+
 int acache_write_slots(const acache_attn_desc* desc, int batch, int rows,
                        const int32_t* write_slot, const void* k_new, const void* v_new,
                        void* k_cache, void* v_cache, int64_t num_slots, int64_t private_begin,
@@ -247,6 +279,31 @@ int acache_slot_attention(const acache_attn_desc* desc, int batch, int n_q, cons
                           int32_t* dev_status, void* stream) {
     return slot_attention(desc, batch, n_q, q, seq_len, read_slot, k_cache, v_cache, num_slots, out,
                           dev_status, stream, false);
+}
+
+int acache_slot_attention_varlen(const acache_attn_desc* desc, int batch, const int32_t* q_start,
+                                 int max_q_rows, int total_q_rows, const void* q, const int32_t* kv_start,
+                                 int max_seq_len, const int32_t* read_slot, const void* k_cache,
+                                 const void* v_cache, int64_t num_slots, void* out, int drop_none,
+                                 int32_t* dev_status, void* stream_) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (batch < 0 || max_q_rows < 0 || total_q_rows < 0 || max_seq_len < 0 || num_slots < 0)
+        return ACACHE_ERR_INVALID_ARG;
+    if (batch == 0 || max_q_rows == 0 || total_q_rows == 0) return ACACHE_OK;
+    if (max_seq_len == 0) return ACACHE_ERR_INVALID_ARG;   // a softmax over no keys
+    if (!q_start || !kv_start || !q || !read_slot || !k_cache || !v_cache || !out)
+        return ACACHE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return ACACHE_ERR_INVALID_ARG;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (tc_supported(a))
+        return launch_tc_slot_attention_varlen(a, batch, q_start, max_q_rows, total_q_rows, q, kv_start,
+                                               max_seq_len, read_slot, k_cache, v_cache, num_slots, out,
+                                               dev_status, stream, drop_none != 0);
+    return launch_simt_slot_attention_varlen(a, batch, q_start, max_q_rows, q, kv_start, max_seq_len,
+                                             read_slot, k_cache, v_cache, num_slots, out, dev_status,
+                                             stream, drop_none != 0);
 }
 
 int acache_slot_attention_dropna(const acache_attn_desc* desc, int batch, int n_q, const void* q,

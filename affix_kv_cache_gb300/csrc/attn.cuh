@@ -24,12 +24,15 @@ struct SlotKeys {
     int hkv;
     int d;
     bool drop_none;
+    const int32_t* kv_start;   // ragged batches: [B+1] offsets of each request's entries, or null
+    ACACHE_DEVFN int64_t base(int b) const { return kv_start ? (int64_t)kv_start[b] : (int64_t)b * T_len; }
+    ACACHE_DEVFN int len(int b) const { return kv_start ? kv_start[b + 1] - kv_start[b] : T_len; }
     ACACHE_DEVFN bool dropped(int b, int t) const {
-        return drop_none && read_slot[(int64_t)b * T_len + t] == ACACHE_SLOT_NONE;
+        return drop_none && read_slot[base(b) + t] == ACACHE_SLOT_NONE;
     }
     ACACHE_DEVFN bool rows(int b, int t, int hk, const T*& kr, const T*& vr,
                            int32_t* dev_status) const {
-        const int64_t s = read_slot[(int64_t)b * T_len + t];
+        const int64_t s = read_slot[base(b) + t];
         if (s < 0 || s >= num_slots) {
             flag(dev_status, ACACHE_DEV_BAD_SLOT);
             return false;
@@ -42,7 +45,7 @@ struct SlotKeys {
     // Element offset of key t's row (same for K and V) in source `src`, or -1 (zero row).
     ACACHE_DEVFN int64_t locate(int b, int t, int hk, int& src, int32_t* dev_status) const {
         src = 0;
-        const int64_t s = read_slot[(int64_t)b * T_len + t];
+        const int64_t s = read_slot[base(b) + t];
         if (s < 0 || s >= num_slots) {
             flag(dev_status, ACACHE_DEV_BAD_SLOT);
             return -1;
@@ -63,6 +66,7 @@ struct ProbeKeys {
     const T* v_aff;
     int l, L, P, hkv, d;
     ACACHE_DEVFN bool dropped(int, int) const { return false; }
+    ACACHE_DEVFN int len(int) const { return P + L; }
     ACACHE_DEVFN bool rows(int b, int t, int hk, const T*& kr, const T*& vr, int32_t*) const {
         if (t >= l && t < l + L) {
             const int64_t off = ((int64_t)(t - l) * hkv + hk) * d;
@@ -95,6 +99,12 @@ int launch_simt_slot_attention(const AttnArgs& a, int B, int n_q, const void* q,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
                                int64_t num_slots, void* out, int32_t* dev_status,
                                cudaStream_t stream, bool drop_none = false);
+// Ragged batches (see launch_tc_slot_attention_varlen).
+int launch_simt_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_start, int max_q,
+                                      const void* q, const int32_t* kv_start, int max_T,
+                                      const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                                      int64_t num_slots, void* out, int32_t* dev_status,
+                                      cudaStream_t stream, bool drop_none);
 int launch_simt_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                              const void* k_req, const void* v_req, const void* k_aff,
                              const void* v_aff, void* out, float* stat_m, float* stat_l,

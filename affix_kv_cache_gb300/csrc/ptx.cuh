@@ -209,6 +209,13 @@ ACACHE_DEVFN void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
 ACACHE_DEVFN void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 ACACHE_DEVFN void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---- programmatic dependent launch ---------------------------------------------------------
+// In a grid launched with programmatic stream serialisation: wait until the preceding grid on
+// the stream has completed and its memory writes are visible (a no-op otherwise).
+ACACHE_DEVFN void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid on the stream start its prologue before this grid has finished.
+ACACHE_DEVFN void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- thread-block clusters (distributed shared memory) ------------------------------------
 ACACHE_DEVFN uint32_t cluster_ctarank() {
     uint32_t r;

@@ -25,7 +25,8 @@ template <typename T, int D, typename Keys>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 simt_attention_kernel(Keys keys, const T* __restrict__ q, T* __restrict__ out, int B, int n_rows,
                       int Hq, int Hkv, int T_len, float scale_log2, float* __restrict__ stat_m,
-                      float* __restrict__ stat_l, int32_t* dev_status) {
+                      float* __restrict__ stat_l, int32_t* dev_status,
+                      const int32_t* __restrict__ q_start) {
     static_assert(D % 32 == 0, "head dim must be a multiple of 32");
     constexpr int kPer = D / 32;
     __shared__ float qs[kWarpsPerBlock][D];
@@ -36,7 +37,20 @@ simt_attention_kernel(Keys keys, const T* __restrict__ q, T* __restrict__ out, i
     const int h = (int)((gw / n_rows) % Hq);
     const int b = (int)(gw / ((int64_t)n_rows * Hq));
     const int hk = h / (Hq / Hkv);
-    const int64_t qoff = (((int64_t)b * n_rows + i) * Hq + h) * D;
+    // ragged batches: request b owns query rows [q_start[b], q_start[b+1]) and keys.len(b)
+    // logical keys; n_rows and T_len are then the largest per-request counts
+    int64_t qrow = (int64_t)b * n_rows + i;
+    if (q_start) {
+        const int nb = q_start[b + 1] - q_start[b], tb = keys.len(b);
+        if (nb != 0 && (nb < 0 || nb > n_rows || tb < 1 || tb > T_len)) {
+            if (i == 0 && h == 0 && lane == 0) flag(dev_status, ACACHE_DEV_BAD_LENGTH);
+            return;
+        }
+        if (i >= nb) return;
+        qrow = q_start[b] + i;
+        T_len = tb;
+    }
+    const int64_t qoff = (qrow * Hq + h) * D;
     for (int c = lane; c < D; c += 32) qs[warp][c] = to_f32(q[qoff + c]);
     __syncwarp();
 
@@ -126,13 +140,13 @@ simt_probe_colsum_kernel(const T* __restrict__ q, const T* __restrict__ k_aff,
 template <typename T, int D, typename Keys>
 int launch_simt(Keys keys, const void* q, void* out, int B, int n_rows, int Hq, int Hkv, int T_len,
                 float scale_log2, float* stat_m, float* stat_l, int32_t* dev_status,
-                cudaStream_t stream) {
+                cudaStream_t stream, const int32_t* q_start = nullptr) {
     const int64_t warps = (int64_t)B * Hq * n_rows;
     if (warps == 0) return ACACHE_OK;
     const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     simt_attention_kernel<T, D, Keys><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(
         keys, (const T*)q, (T*)out, B, n_rows, Hq, Hkv, T_len, scale_log2, stat_m, stat_l,
-        dev_status);
+        dev_status, q_start);
     return launch_status();
 }
 
@@ -154,9 +168,22 @@ int launch_simt_slot_attention(const AttnArgs& a, int B, int n_q, const void* q,
                                cudaStream_t stream, bool drop_none) {
     ACACHE_DISPATCH_TD(a.dtype, a.d, {
         SlotKeys<T> keys{(const T*)k_cache, (const T*)v_cache, read_slot, num_slots, T_len, a.hkv, D,
-                         drop_none};
+                         drop_none, nullptr};
         return launch_simt<T, D>(keys, q, out, B, n_q, a.hq, a.hkv, T_len, a.scale * kLog2e,
                                  nullptr, nullptr, dev_status, stream);
+    });
+}
+
+int launch_simt_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_start, int max_q,
+                                      const void* q, const int32_t* kv_start, int max_T,
+                                      const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                                      int64_t num_slots, void* out, int32_t* dev_status,
+                                      cudaStream_t stream, bool drop_none) {
+    ACACHE_DISPATCH_TD(a.dtype, a.d, {
+        SlotKeys<T> keys{(const T*)k_cache, (const T*)v_cache, read_slot, num_slots, max_T, a.hkv, D,
+                         drop_none, kv_start};
+        return launch_simt<T, D>(keys, q, out, B, max_q, a.hq, a.hkv, max_T, a.scale * kLog2e,
+                                 nullptr, nullptr, dev_status, stream, q_start);
     });
 }
 

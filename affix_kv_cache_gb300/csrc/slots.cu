@@ -9,6 +9,7 @@
 // count.  Slot indices are read once per 16-byte chunk (they hit L1: all chunks of a
 // row share one index).
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace acache {
 namespace {
@@ -25,6 +26,9 @@ indexed_row_copy(const int32_t* __restrict__ idx, int64_t nrows, int64_t cpr,
                  const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
                  uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
                  int64_t num_slots, int64_t private_begin, int32_t* dev_status) {
+    // a grid that waits on this copy (store-then-attend) may start its prologue now; it
+    // reads nothing this copy writes before its own grid-dependency wait
+    ptx::grid_launch_dependents();
     const int64_t total = nrows * cpr;                   // chunks per tensor (K or V)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < 2 * total;

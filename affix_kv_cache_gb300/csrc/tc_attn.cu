@@ -84,6 +84,8 @@ struct AttnParams {
     CUtensorMap tm_k1;    // probe: 4-D own rows [B][P][Hkv][d], box {64, 1, 128, 1}
     CUtensorMap tm_v1;
     const int32_t* read_slot;
+    const int32_t* q_start;   // ragged batches (slot keys): [B+1] query-row offsets, or null
+    const int32_t* kv_start;  //                              [B+1] logical-key offsets
     bf16* out;
     float* stat_m;
     float* stat_l;
@@ -128,13 +130,13 @@ ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_f
 // cover the affix rows first, then the request's own rows: the order of keys inside a row
 // does not change the softmax.
 template <int kMode>
-ACACHE_DEVFN int n_key_tiles(const AttnParams& p) {
-    if (kMode == kSlotKeys) return (p.T_len + kBN - 1) / kBN;
+ACACHE_DEVFN int n_key_tiles(const AttnParams& p, int T_len) {
+    if (kMode == kSlotKeys) return (T_len + kBN - 1) / kBN;
     return (p.L + kBN - 1) / kBN + (p.P + kBN - 1) / kBN;
 }
 template <int kMode>
-ACACHE_DEVFN int tile_valid(const AttnParams& p, int j) {
-    if (kMode == kSlotKeys) return min(kBN, p.T_len - j * kBN);
+ACACHE_DEVFN int tile_valid(const AttnParams& p, int j, int T_len) {
+    if (kMode == kSlotKeys) return min(kBN, T_len - j * kBN);
     const int n_aff = (p.L + kBN - 1) / kBN;
     return j < n_aff ? min(kBN, p.L - j * kBN) : min(kBN, p.P - (j - n_aff) * kBN);
 }
@@ -160,9 +162,25 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     const int h = bh % p.Hq;
     const int b = bh / p.Hq;
     const int hk = h / (p.Hq / p.Hkv);
+    // Ragged batches (read-slot keys): request b owns query rows [q_start[b], q_start[b+1]) and
+    // read-slot entries [kv_start[b], kv_start[b+1]) of the flattened tensors; p.n_rows and
+    // p.T_len are then the largest per-request counts.  A CTA without rows leaves at once.
+    int n_rows = p.n_rows, T_len = p.T_len;
+    int64_t qbase = (int64_t)b * p.n_rows, kbase = (int64_t)b * p.T_len;
+    if (kMode == kSlotKeys && p.q_start) {
+        qbase = p.q_start[b];
+        kbase = p.kv_start[b];
+        n_rows = (int)(p.q_start[b + 1] - qbase);
+        T_len = (int)(p.kv_start[b + 1] - kbase);
+        if (n_rows != 0 && (n_rows < 0 || n_rows > p.n_rows || T_len < 1 || T_len > p.T_len)) {
+            if (threadIdx.x == 0 && qb == 0 && h == 0) flag(p.dev_status, ACACHE_DEV_BAD_LENGTH);
+            return;
+        }
+    }
     const int q0 = qb * kQT * kBM;
-    const int n_qt = min(kQT, (p.n_rows - q0 + kBM - 1) / kBM);   // Q tiles present (1 or 2)
-    const int n_kv = n_key_tiles<kMode>(p);
+    if (q0 >= n_rows) return;
+    const int n_qt = min(kQT, (n_rows - q0 + kBM - 1) / kBM);   // Q tiles present (1 or 2)
+    const int n_kv = n_key_tiles<kMode>(p, T_len);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
@@ -213,8 +231,14 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             }
             mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_qt);
             for (int t = 0; t < n_qt; ++t) {
-                tma_load_4d(sQ(t), &p.tm_q, 0, h, q0 + t * kBM, b, &ctl.q_full);
-                tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, h, q0 + t * kBM, b, &ctl.q_full);
+                if (kMode == kSlotKeys && p.q_start) {   // 3-D map over the flattened rows
+                    const int r = (int)(qbase + q0 + t * kBM);
+                    tma_load_3d(sQ(t), &p.tm_q, 0, h, r, &ctl.q_full);
+                    tma_load_3d(sQ(t) + kRegion, &p.tm_q, 64, h, r, &ctl.q_full);
+                } else {
+                    tma_load_4d(sQ(t), &p.tm_q, 0, h, q0 + t * kBM, b, &ctl.q_full);
+                    tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, h, q0 + t * kBM, b, &ctl.q_full);
+                }
             }
         }
         // warps 12-13 fill the K ring, warps 14-15 the V ring; probe tiles are box loads
@@ -240,8 +264,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 for (int u = 0; u < 4; ++u) {
                     const int t = j * kBN + 4 * g + u;
                     rows[u] = oob_row;
-                    if (kMode == kSlotKeys && j < n_kv && t < p.T_len) {
-                        const int64_t slot = p.read_slot[(int64_t)b * p.T_len + t];
+                    if (kMode == kSlotKeys && j < n_kv && t < T_len) {
+                        const int64_t slot = p.read_slot[kbase + t];
                         if (slot >= 0 && slot < p.num_slots)
                             rows[u] = (int)(slot * p.Hkv + hk);
                         else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
@@ -251,6 +275,9 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             };
             int next[4];
             resolve(0, next);
+            // store-then-attend: the pool rows this launch reads may have been written by the
+            // preceding store grid (launched ahead with programmatic stream serialisation)
+            grid_dependency_wait();
             for (int j = 0; j < n_kv; ++j) {
                 const int s = j % nst;
                 const uint32_t dst_tile = is_v ? sV(s) : sK(s);
@@ -363,11 +390,11 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             // wait for S_t(j), which hides the latency)
             uint32_t drop[4] = {0u, 0u, 0u, 0u};
             if constexpr (kDrop) {
-                const int32_t* rs = p.read_slot + (int64_t)b * p.T_len;
+                const int32_t* rs = p.read_slot + kbase;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int tk = j * kBN + cc * 32 + (threadIdx.x & 31);
-                    drop[cc] = __ballot_sync(0xffffffffu, tk < p.T_len && rs[tk] == ACACHE_SLOT_NONE);
+                    drop[cc] = __ballot_sync(0xffffffffu, tk < T_len && rs[tk] == ACACHE_SLOT_NONE);
                 }
             }
             ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], j & 1, abort_flag, dev_status));
@@ -384,7 +411,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], (t == 0 ? j - 1 : j) & 1,
                                                       abort_flag, dev_status));
             if (!ok) break;
-            const int valid = tile_valid<kMode>(p, j);
+            const int valid = tile_valid<kMode>(p, j, T_len);
             if (valid < kBN) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
@@ -478,13 +505,13 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             tc_fence_after();
             const int i = q0 + t * kBM + r;
             const float inv_l = (kDrop && !(l_sum > 0.f)) ? 0.f : 1.f / l_sum;
-            bf16* orow = p.out ? p.out + (((int64_t)b * p.n_rows + i) * p.Hq + h) * kD : nullptr;
+            bf16* orow = p.out ? p.out + ((qbase + i) * p.Hq + h) * kD : nullptr;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t o[32];
                 tmem_ld32(lane_base + col_o(t) + cc * 32, o);
                 tmem_ld_wait();
-                if (orow && i < p.n_rows) {
+                if (orow && i < n_rows) {
                     uint32_t pkd[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
@@ -694,8 +721,10 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
 }
 
+// pdl: launched with programmatic stream serialisation after a store grid that releases it
+// early (store-then-attend); the producers' grid-dependency wait orders the reads.
 template <int kMode, bool kDrop = false>
-int launch_attn(const AttnParams& prm, int B, cudaStream_t stream) {
+int launch_attn(const AttnParams& prm, int B, cudaStream_t stream, bool pdl = false) {
     const int64_t ctas = (int64_t)B * prm.Hq * ((prm.n_rows + kQT * kBM - 1) / (kQT * kBM));
     if (ctas == 0) return ACACHE_OK;
     if (ctas > 0x7fffffff) return ACACHE_ERR_INVALID_ARG;
@@ -704,7 +733,24 @@ int launch_attn(const AttnParams& prm, int B, cudaStream_t stream) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
     }
-    kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(prm);
+    if (!pdl) {
+        kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(prm);
+        return launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ACACHE_ERR_CUDA;
+    }
     return launch_status();
 }
 
@@ -715,7 +761,7 @@ bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == k
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
-                             cudaStream_t stream, bool drop_none) {
+                             cudaStream_t stream, bool drop_none, bool pdl) {
     if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
         return ACACHE_ERR_INVALID_ARG;
     AttnParams prm{};
@@ -734,6 +780,35 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
     prm.T_len = T_len;
+    prm.scale_log2 = a.scale * kLog2e;
+    return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream, pdl)
+                     : launch_attn<kSlotKeys>(prm, B, stream, pdl);
+}
+
+int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_start, int max_q,
+                                    int total_q, const void* q, const int32_t* kv_start, int max_T,
+                                    const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                                    int64_t num_slots, void* out, int32_t* dev_status,
+                                    cudaStream_t stream, bool drop_none) {
+    if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || total_q < 0) return ACACHE_ERR_INVALID_ARG;
+    AttnParams prm{};
+    const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)(total_q > 0 ? total_q : 1)};
+    const uint64_t dp[2] = {(uint64_t)kD, (uint64_t)num_slots * a.hkv};
+    if (!make_map(&prm.tm_q, q, 3, dq, 2, kBM) || !make_map(&prm.tm_k0, k_cache, 2, dp, 1, 1) ||
+        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1))
+        return ACACHE_ERR_CUDA;
+    prm.tm_k1 = prm.tm_k0;
+    prm.tm_v1 = prm.tm_v0;
+    prm.read_slot = read_slot;
+    prm.q_start = q_start;
+    prm.kv_start = kv_start;
+    prm.out = (bf16*)out;
+    prm.dev_status = dev_status;
+    prm.num_slots = num_slots;
+    prm.n_rows = max_q;
+    prm.Hq = a.hq;
+    prm.Hkv = a.hkv;
+    prm.T_len = max_T;
     prm.scale_log2 = a.scale * kLog2e;
     return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream) : launch_attn<kSlotKeys>(prm, B, stream);
 }

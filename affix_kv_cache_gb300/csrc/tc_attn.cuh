@@ -22,14 +22,22 @@ bool tc_supported(const AttnArgs& a);
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
-                             cudaStream_t stream, bool drop_none = false);
+                             cudaStream_t stream, bool drop_none = false, bool pdl = false);
+// Ragged batches: request b's query rows are [q_start[b], q_start[b+1]) of q / out
+// ([total_q][Hq][d]) and its logical keys read_slot[kv_start[b] .. kv_start[b+1]); max_q and
+// max_T bound the per-request counts (a request outside them is skipped and flagged).
+int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_start, int max_q,
+                                    int total_q, const void* q, const int32_t* kv_start, int max_T,
+                                    const int32_t* read_slot, const void* k_cache, const void* v_cache,
+                                    int64_t num_slots, void* out, int32_t* dev_status,
+                                    cudaStream_t stream, bool drop_none);
 // Block-decode form of the read-slot attention (few query rows per KV head): true when it
 // streams fewer K/V tiles than the recompute-point kernel for this geometry.
 bool tc_decode_preferred(const AttnArgs& a, int n_q);
 int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
                                int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream,
-                               bool drop_none = false);
+                               bool drop_none = false, bool pdl = false);
 int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                            const void* k_req, const void* v_req, const void* k_aff,
                            const void* v_aff, void* out, float* stat_m, float* stat_l,

@@ -212,6 +212,8 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
         };
         int next[4];
         resolve(0, next);
+        // store-then-attend: wait for the preceding store grid before reading the pool
+        grid_dependency_wait();
         for (int j = 0; j < n_kv; ++j) {
             const int s = j % kStages;
             int rows[4] = {next[0], next[1], next[2], next[3]};
@@ -563,7 +565,7 @@ int prepare(int dev) {
 }
 
 template <int REP, bool kDrop>
-int launch_rep(const DecParams& prm, int64_t ctas, cudaStream_t stream) {
+int launch_rep(const DecParams& prm, int64_t ctas, cudaStream_t stream, bool pdl) {
     auto kern = tc_decode_kernel<REP, kDrop>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -576,13 +578,22 @@ int launch_rep(const DecParams& prm, int64_t ctas, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)prm.cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (prm.cs > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)prm.cs;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = prm.cs > 1 ? 1 : 0;
+    cfg.numAttrs = na;
     if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
@@ -608,7 +619,7 @@ bool tc_decode_preferred(const AttnArgs& a, int n_q) {
 int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
                                int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream,
-                               bool drop_none) {
+                               bool drop_none, bool pdl) {
     if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
         return ACACHE_ERR_INVALID_ARG;
     const int g = a.hq / a.hkv;
@@ -639,15 +650,15 @@ int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q,
     prm.scale_log2 = a.scale * kLog2e;
     if (drop_none) {
         switch (dg.rep) {
-            case 4: return launch_rep<4, true>(prm, ctas, stream);
-            case 2: return launch_rep<2, true>(prm, ctas, stream);
-            default: return launch_rep<1, true>(prm, ctas, stream);
+            case 4: return launch_rep<4, true>(prm, ctas, stream, pdl);
+            case 2: return launch_rep<2, true>(prm, ctas, stream, pdl);
+            default: return launch_rep<1, true>(prm, ctas, stream, pdl);
         }
     }
     switch (dg.rep) {
-        case 4: return launch_rep<4, false>(prm, ctas, stream);
-        case 2: return launch_rep<2, false>(prm, ctas, stream);
-        default: return launch_rep<1, false>(prm, ctas, stream);
+        case 4: return launch_rep<4, false>(prm, ctas, stream, pdl);
+        case 2: return launch_rep<2, false>(prm, ctas, stream, pdl);
+        default: return launch_rep<1, false>(prm, ctas, stream, pdl);
     }
 }
 

@@ -65,7 +65,8 @@ enum {
     ACACHE_DEV_BAD_ROW = 4,       /* a masked-row index outside [0, P)                     */
     ACACHE_DEV_BAD_ANCHOR = 8,    /* anchors not strictly ascending offsets in [0, L)      */
     ACACHE_DEV_NAN = 16,          /* a NaN importance score reached Top-K                  */
-    ACACHE_DEV_TIMEOUT = 32       /* a bounded wait inside a kernel gave up                */
+    ACACHE_DEV_TIMEOUT = 32,      /* a bounded wait inside a kernel gave up                */
+    ACACHE_DEV_BAD_LENGTH = 64    /* a ragged-batch request length outside its bounds     */
 };
 
 /* Read-slot map entry of a logical position whose K/V was discarded (the page's DropNA
@@ -205,6 +206,24 @@ ACACHE_API int acache_write_slots(const acache_attn_desc* a, int batch, int rows
                        int64_t private_begin, int32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * (4a+4b) Store-then-attend of one layer in one call.  Page: Sec. 4.3 and App. C.1 (the
+ * same store-then-attend interface at recompute points and in block decoding: write the
+ * fresh K/V through the write-side map, then attend through the read-slot map).
+ * Exactly acache_write_slots(rows, write_slot, k_new, v_new, ...) followed by
+ * acache_slot_attention(n_q, q, seq_len, read_slot, ...) on the same pools, with the same
+ * arguments, layouts and errors (every argument is checked before anything is launched).
+ * On the tensor-core path the attention grid is launched with programmatic stream
+ * serialisation: its set-up and query loads overlap the store, and it waits for the store
+ * to complete before it reads any key or value row.  rows = 0 attends only; n_q = 0
+ * stores only.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_store_attend(const acache_attn_desc* a, int batch, int rows,
+                        const int32_t* write_slot, const void* k_new, const void* v_new,
+                        void* k_cache, void* v_cache, int64_t num_slots, int64_t private_begin,
+                        int n_q, const void* q, int seq_len, const int32_t* read_slot, void* out,
+                        int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * (4b) Read-slot attention of one layer.  Page: Sec. 4.3 (queries only for recomputed
  * positions, keys and values read through the read-slot map) and App. C.1.
  * Each of the n_q dense query rows of request b attends bidirectionally over all T
@@ -232,6 +251,27 @@ ACACHE_API int acache_slot_attention_dropna(const acache_attn_desc* a, int batch
                           const void* q, int seq_len, const int32_t* read_slot,
                           const void* k_cache, const void* v_cache, int64_t num_slots, void* out,
                           int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * (4b'') Read-slot attention over a ragged batch.  Page: App. C.1 (the prototype's kernel
+ * takes ragged query and KV lengths besides the read-slot map) and Sec. 4.3.
+ * The computation of acache_slot_attention, with per-request row counts:
+ *   q_start  [B+1] int32 (device): request b's query rows are q_start[b] .. q_start[b+1]-1
+ *            of q and out ([total_q_rows][Hq][d], total_q_rows = q_start[B])
+ *   kv_start [B+1] int32 (device): request b's logical keys are the read-slot entries
+ *            read_slot[kv_start[b] .. kv_start[b+1]-1] (one flattened int32 array)
+ *   max_q_rows, max_seq_len (host): bounds on every request's row and key counts; the
+ *            launch is sized by them.  total_q_rows (host) sizes the query tensor map.
+ * A request with zero query rows is skipped.  A request whose counts are negative, above
+ * the bounds, or that has rows but no key is skipped (its output rows are not written) and
+ * flagged ACACHE_DEV_BAD_LENGTH.  drop_none != 0 gives ACACHE_SLOT_NONE the DropNA meaning
+ * of acache_slot_attention_dropna.  Other errors as acache_slot_attention.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_slot_attention_varlen(const acache_attn_desc* a, int batch,
+                          const int32_t* q_start, int max_q_rows, int total_q_rows, const void* q,
+                          const int32_t* kv_start, int max_seq_len, const int32_t* read_slot,
+                          const void* k_cache, const void* v_cache, int64_t num_slots, void* out,
+                          int drop_none, int32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Logical KV view.  Page: Sec. 4.1 ("the same logical full-context KV view").
