@@ -32,7 +32,9 @@ EXPORTS = ("acache_status_string", "acache_version", "acache_probe_workspace_byt
            "acache_probe_scores", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
            "acache_write_slots", "acache_slot_attention", "acache_gather_slots",
            "acache_kv_deviation_scores", "acache_slot_attention_dropna", "acache_slot_attention_varlen",
-           "acache_store_attend")
+           "acache_store_attend", "acache_rerotate_keys", "acache_pool_create", "acache_pool_destroy",
+           "acache_pool_register_affix", "acache_pool_release_affix", "acache_pool_alloc_private",
+           "acache_pool_free_private", "acache_pool_stats")
 
 
 class AcacheError(RuntimeError):
@@ -83,6 +85,16 @@ def lib() -> ctypes.CDLL:
             "acache_slot_attention_dropna": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
             "acache_slot_attention_varlen": (I, [D, I, P, I, I, P, P, I, P, P, P, I64, P, I, P, P]),
             "acache_store_attend": (I, [D, I, I, P, P, P, P, P, I64, I64, I, P, I, P, P, P, P]),
+            "acache_rerotate_keys": (I, [D, I64, P, P, ctypes.c_int32, ctypes.c_double, I, P]),
+            "acache_pool_create": (I, [I64, I64, ctypes.c_int32, ctypes.POINTER(P)]),
+            "acache_pool_destroy": (None, [P]),
+            "acache_pool_register_affix": (I, [P, ctypes.c_uint64, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                               ctypes.POINTER(ctypes.c_int32)]),
+            "acache_pool_release_affix": (I, [P, ctypes.c_uint64]),
+            "acache_pool_alloc_private": (I, [P, ctypes.c_int32, P, ctypes.POINTER(I64)]),
+            "acache_pool_free_private": (I, [P, I64]),
+            "acache_pool_stats": (I, [P, ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_int32),
+                                      ctypes.POINTER(ctypes.c_int32)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -228,3 +240,60 @@ def acache_store_attend(desc, batch, rows, write_slot, k_new, v_new, k_cache, v_
                                    _p(k_cache), _p(v_cache), num_slots, private_begin, n_q, _p(q),
                                    seq_len, _p(read_slot), _p(out), _p(dev_status), _stream(stream))
     return _check("acache_store_attend", st) if check else st
+
+
+def acache_rerotate_keys(desc, rows, k_in, k_out, delta_pos, rope_theta, interleaved=False, stream=None,
+                         check=True):
+    """Move rotary-embedded keys [rows][Hkv][d] by delta_pos positions (see include/acache.h)."""
+    st = lib().acache_rerotate_keys(ctypes.byref(desc), rows, _p(k_in), _p(k_out), int(delta_pos),
+                                    float(rope_theta), int(bool(interleaved)), _stream(stream))
+    return _check("acache_rerotate_keys", st) if check else st
+
+
+class Pool:
+    """Host-side admission runtime of one KV slot layout (include/acache.h, acache_pool_*):
+    the shared-affix registry and the private-page allocator.  Marshalling only."""
+
+    def __init__(self, num_slots, private_begin, page_slots):
+        h = ctypes.c_void_p()
+        _check("acache_pool_create", lib().acache_pool_create(num_slots, private_begin, page_slots,
+                                                              ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            lib().acache_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def register_affix(self, key, affix_len):
+        """Returns (shared_base, created)."""
+        base, created = ctypes.c_int32(), ctypes.c_int32()
+        _check("acache_pool_register_affix", lib().acache_pool_register_affix(
+            self._h, ctypes.c_uint64(key & (2 ** 64 - 1)), affix_len, ctypes.byref(base), ctypes.byref(created)))
+        return base.value, bool(created.value)
+
+    def release_affix(self, key):
+        _check("acache_pool_release_affix", lib().acache_pool_release_affix(self._h, ctypes.c_uint64(key & (2 ** 64 - 1))))
+
+    def alloc_private(self, rows):
+        """Returns (slots as a CPU int32 tensor [rows], request_id)."""
+        slots = torch.empty(rows, dtype=torch.int32)
+        rid = ctypes.c_int64()
+        _check("acache_pool_alloc_private", lib().acache_pool_alloc_private(
+            self._h, rows, ctypes.c_void_p(slots.data_ptr()) if rows else None, ctypes.byref(rid)))
+        return slots, rid.value
+
+    def free_private(self, request_id):
+        _check("acache_pool_free_private", lib().acache_pool_free_private(self._h, request_id))
+
+    def stats(self):
+        fs, fp, na, nr = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check("acache_pool_stats", lib().acache_pool_stats(self._h, ctypes.byref(fs), ctypes.byref(fp),
+                                                            ctypes.byref(na), ctypes.byref(nr)))
+        return {"free_shared": fs.value, "free_private": fp.value, "affixes": na.value, "requests": nr.value}

@@ -208,6 +208,17 @@ int acache_kv_deviation_scores(const acache_attn_desc* desc, int batch, int affi
                                v_full, scores, (cudaStream_t)stream);
 }
 
+int acache_rerotate_keys(const acache_attn_desc* desc, int64_t rows, const void* k_in, void* k_out,
+                         int32_t delta_pos, double rope_theta, int interleaved, void* stream) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (rows < 0 || !(rope_theta > 0.0) || isinf(rope_theta)) return ACACHE_ERR_INVALID_ARG;
+    if (rows == 0) return ACACHE_OK;
+    if (!k_in || !k_out || !aligned16(k_in) || !aligned16(k_out)) return ACACHE_ERR_INVALID_ARG;
+    return launch_rerotate(a.dtype, rows, a.hkv, a.d, k_in, k_out, delta_pos, rope_theta, interleaved != 0,
+                           (cudaStream_t)stream);
+}
+
 int acache_build_slot_maps(int batch, int seq_len, int affix_begin, int affix_len, int k,
                            const int32_t* anchors, const int32_t* shared_slot,
                            const int32_t* private_slots, int32_t* write_pos, int32_t* read_slot,

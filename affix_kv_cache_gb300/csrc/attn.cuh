@@ -129,6 +129,8 @@ int launch_build_maps(int batch, int T, int l, int L, int K, const int32_t* anch
                       cudaStream_t stream);
 int launch_topk(const float* scores, int batch, int L, int K, int32_t* anchors,
                 int32_t* dev_status, cudaStream_t stream);
+int launch_rerotate(int dtype, int64_t rows, int hkv, int d, const void* k_in, void* k_out, int32_t delta,
+                    double theta, int interleaved, cudaStream_t stream);
 int launch_kv_deviation(int dtype, int B, int L, int Hkv, int d, const void* k_sh, const void* v_sh,
                         const void* k_full, const void* v_full, float* scores, cudaStream_t stream);
 

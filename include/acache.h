@@ -283,6 +283,56 @@ ACACHE_API int acache_gather_slots(const acache_attn_desc* a, int batch, int seq
                         int64_t num_slots, void* k_out, void* v_out, int32_t* dev_status,
                         void* stream);
 
+/* ---------------------------------------------------------------------------------
+ * Position-aware affix registration.  Page: Sec. 4 (opening) and Limitations -- the cache
+ * is kept after the rotary position rotation, so reusing a shared affix at another offset
+ * needs its keys moved to the new positions.  Rotations compose: a key rotated for position
+ * p becomes the key for position p + delta_pos after one more rotation by delta_pos x the
+ * pair's frequency rope_theta^(-2i/d).  Values are unchanged.
+ *   k_in, k_out [rows][Hkv][d] (may be the same buffer), 16-byte aligned
+ *   interleaved = 0: pair i is (x_i, x_{i+d/2}) (rotate-half layout); 1: (x_{2i}, x_{2i+1})
+ * cos/sin are computed on the host in double precision; the rotation runs in float32 and is
+ * rounded once to the storage type.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_rerotate_keys(const acache_attn_desc* a, int64_t rows, const void* k_in,
+                        void* k_out, int32_t delta_pos, double rope_theta, int interleaved,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Admission runtime (host only; no device memory is touched).  Page: Sec. 4.1-4.2 -- the
+ * shared region stores each common affix once and later compatible requests reuse it; each
+ * request gets private slots for its anchors and its own positions; admission resolves the
+ * affix and records the maps before the online loop.
+ *
+ * A pool describes the slot layout shared by every layer's KV pool: slots
+ * [0, private_begin) are the shared region, [private_begin, num_slots) private pages of
+ * page_slots slots (a partial last page is not used).  All functions are thread-safe.
+ *   create:   *out receives the handle (ACACHE_ERR_WORKSPACE if host memory runs out).
+ *   register_affix: the affix identified by the caller's 64-bit key (for instance a hash of
+ *             its token ids and its offset) gets affix_len contiguous shared slots starting
+ *             at *shared_base.  *created = 1 the first time: the caller then writes the
+ *             affix's K/V there (acache_write_slots with private_begin = 0); later calls with
+ *             the same key only add a reference (*created = 0).  A known key with another
+ *             length is ACACHE_ERR_INVALID_ARG; a full shared region ACACHE_ERR_WORKSPACE.
+ *   release_affix: drops one reference; the slots are free again at zero references.
+ *   alloc_private: slots[0..rows) (host array) receives the private slots of a new request,
+ *             page by page; *request_id identifies it.  ACACHE_ERR_WORKSPACE when pages run out.
+ *   free_private: returns the request's pages.
+ *   stats:    free shared / private slots, live affixes and requests (any pointer may be NULL).
+ * ------------------------------------------------------------------------------- */
+typedef struct acache_pool acache_pool;
+ACACHE_API int acache_pool_create(int64_t num_slots, int64_t private_begin, int32_t page_slots,
+                        acache_pool** out);
+ACACHE_API void acache_pool_destroy(acache_pool* pool);
+ACACHE_API int acache_pool_register_affix(acache_pool* pool, uint64_t key, int32_t affix_len,
+                        int32_t* shared_base, int32_t* created);
+ACACHE_API int acache_pool_release_affix(acache_pool* pool, uint64_t key);
+ACACHE_API int acache_pool_alloc_private(acache_pool* pool, int32_t rows, int32_t* slots,
+                        int64_t* request_id);
+ACACHE_API int acache_pool_free_private(acache_pool* pool, int64_t request_id);
+ACACHE_API int acache_pool_stats(acache_pool* pool, int64_t* free_shared_slots,
+                        int64_t* free_private_slots, int32_t* n_affixes, int32_t* n_requests);
+
 #ifdef __cplusplus
 }
 #endif

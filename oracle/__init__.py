@@ -59,10 +59,11 @@ def _load():
             lib.ref_slot_attention.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P, L, P, I, I, P]
             lib.ref_dense_attention.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P]
             lib.ref_kv_deviation.argtypes = [I, I, I, I, I, P, P, P, P, P]
+            lib.ref_rerotate.argtypes = [L, I, I, I, P, I, D, I, P]
             lib.ref_set_threads.argtypes = [I]
             for f in ("ref_probe_layer", "ref_topk", "ref_build_slot_maps", "ref_write_slots",
                       "ref_gather_slots", "ref_slot_attention", "ref_dense_attention",
-                      "ref_kv_deviation",
+                      "ref_kv_deviation", "ref_rerotate",
                       "ref_version", "ref_get_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -251,3 +252,15 @@ def kv_deviation(k_shared, v_shared, k_full, v_full, scores=None):
     if rc != 0:
         raise ValueError("ref_kv_deviation rejected its arguments")
     return sc
+
+
+def rerotate(k, delta, theta, interleaved=False):
+    """Reading R8: keys k [rows][Hkv][d] carrying the rotary rotation of some position, moved
+    by ``delta`` positions.  Returns float64 [rows][Hkv][d]."""
+    ka, dt = _raw(k)
+    rows, Hkv, d = ka.shape
+    out = np.zeros((rows, Hkv, d), np.float64)
+    rc = _load().ref_rerotate(rows, Hkv, d, dt, _p(ka), int(delta), float(theta), int(bool(interleaved)), _p(out))
+    if rc != 0:
+        raise ValueError("ref_rerotate rejected its arguments")
+    return out

@@ -30,6 +30,9 @@
  *       inside the full prompt moved from the affix-only cache; the measure taken is the
  *       L2 norm of the key difference plus that of the value difference, per KV head,
  *       summed over KV heads and layers.
+ *   R8  Position-aware affix registration (Sec. 4 opening, Limitations): a cached key that
+ *       carries the rotary rotation of position p is moved to p + delta by rotating every
+ *       frequency pair i (frequency theta^(-2i/d)) by delta times that frequency.
  *   R7  DropNA (Sec. 5.3) throws away the cached K/V of every non-anchor affix position:
  *       such a position has no key at all -- it is left out of the softmax, not read as a
  *       zero row; a row left with no key outputs zeros.
@@ -414,5 +417,27 @@ int ref_kv_deviation(int B, int L, int Hkv, int d, int dtype, const void* k_sh, 
             }
             scores[(int64_t)b * L + j] += dev;
         }
+    return 0;
+}
+
+/*
+ * Re-rotation of rotary-embedded keys (reading R8).  k [rows][Hkv][d] -> out (double).
+ * Pair i is (x_i, x_{i + d/2}) when interleaved == 0, (x_{2i}, x_{2i+1}) otherwise; the pair
+ * (a, b) becomes (a cos w - b sin w, a sin w + b cos w) with w = delta * theta^(-2i/d).
+ */
+int ref_rerotate(int64_t rows, int Hkv, int d, int dtype, const void* k, int delta, double theta,
+                 int interleaved, double* out) {
+    if (rows < 0 || Hkv <= 0 || d <= 0 || d % 2 || !(theta > 0.0)) return -1;
+    for (int64_t r = 0; r < rows * Hkv; ++r) {
+        const int64_t off = r * d;
+        for (int i = 0; i < d / 2; ++i) {
+            const int ia = interleaved ? 2 * i : i;
+            const int ib = interleaved ? 2 * i + 1 : i + d / 2;
+            const double w = (double)delta * pow(theta, -2.0 * (double)i / (double)d);
+            const double a = widen(k, dtype, off + ia), b = widen(k, dtype, off + ib);
+            out[off + ia] = a * cos(w) - b * sin(w);
+            out[off + ib] = a * sin(w) + b * cos(w);
+        }
+    }
     return 0;
 }
