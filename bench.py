@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the block-decode measurement")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-launch measurements of the other workloads (Dream GQA infix, paged "
+                         "LLaDA decode, long suffix with its ratio and batch sweeps), one JSON line each")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle sample")
     ap.add_argument("--layers", type=int, default=0,
@@ -277,6 +280,10 @@ class Decode:
             if "attn" in kinds:
                 ac.acache_slot_attention(p.desc, w.batch, self.n, d["q_blk"], w.T, p.read_slot,
                                          p.kc[n], p.vc[n], p.lay.num_slots, self.out)
+            if "fused" in kinds:
+                ac.acache_store_attend(p.desc, w.batch, self.n, self.wslot[i], d["k_blk"], d["v_blk"],
+                                       p.kc[n], p.vc[n], p.lay.num_slots, p.lay.private_begin, self.n,
+                                       d["q_blk"], w.T, p.read_slot, self.out)
 
     def measure(self, reps, warmup, peaks):
         """Times CUDA-graph replays of STEPS blocks x all layers: the decode loop is
@@ -286,11 +293,17 @@ class Decode:
         torch.cuda.synchronize()
         side = torch.cuda.Stream()
         graphs = {}
-        for name, kinds in (("step", ("write", "attn")), ("attn", ("attn",)), ("write", ("write",))):
+        for name, kinds in (("step", ("write", "attn")), ("attn", ("attn",)), ("write", ("write",)),
+                            ("fused", ("fused",))):
             g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=side):
-                for i in range(self.STEPS):
-                    self.run(i, kinds)
+            try:
+                with torch.cuda.graph(g, stream=side):
+                    for i in range(self.STEPS):
+                        self.run(i, kinds)
+            except Exception as e:   # a capture the driver refuses is reported, not fatal
+                graphs[name] = None
+                print(f"decode: capture of {name} failed: {e}", file=sys.stderr)
+                continue
             graphs[name] = g
         torch.cuda.synchronize()
         w = self.p.w
@@ -308,12 +321,14 @@ class Decode:
             return a.elapsed_time(b) / reps
 
         t_step, t_attn, t_write = (replay_ms(graphs[k]) for k in ("step", "attn", "write"))
+        t_fused = replay_ms(graphs["fused"]) if graphs.get("fused") is not None else None
         attn_ms, write_ms = t_attn / per, t_write / per
         achieved = self.unique_bytes / (attn_ms / 1e3) / 1e9
         return {
             "workload": w.name, "block": self.n, "layers": w.layers, "replays": reps,
             "timing": f"CUDA graph replay, {per} launches of each kind per replay",
             "ms_per_layer": t_step / per, "attn_ms_per_launch": attn_ms, "write_ms_per_launch": write_ms,
+            "store_attend_ms_per_layer": None if t_fused is None else t_fused / per,
             "attn_tflops": 4.0 * self.n * w.T * w.d * w.hq * w.batch / (attn_ms / 1e3) / 1e12,
             "logical_gather_gbs": self.logical_bytes / (attn_ms / 1e3) / 1e9,
             "write_gbs": self.write_bytes / (write_ms / 1e3) / 1e9,
@@ -322,6 +337,39 @@ class Decode:
                          "peak_source": f"{peaks['source']} HBM copy",
                          "bytes_per_launch": self.unique_bytes, "traffic": None},
         }
+
+
+def store_attend_compare(path, reps=3):
+    """One recompute point over all layers: the store and the attention as two calls, against
+    acache_store_attend (one call; the attention grid starts while the store drains).
+    Returns ms per layer of each, from CUDA events around `reps` passes."""
+    ac, w, lay = path.ac, path.w, path.lay
+
+    def run(fused):
+        for n in range(w.layers):
+            r = path.rec[n]
+            if fused:
+                ac.acache_store_attend(path.desc, w.batch, w.R, lay.private_slots, r["k_new"], r["v_new"],
+                                       path.kc[n], path.vc[n], lay.num_slots, lay.private_begin, w.R,
+                                       r["q_r"], w.T, path.read_slot, path.out[n])
+            else:
+                ac.acache_write_slots(path.desc, w.batch, w.R, lay.private_slots, r["k_new"], r["v_new"],
+                                      path.kc[n], path.vc[n], lay.num_slots, lay.private_begin)
+                ac.acache_slot_attention(path.desc, w.batch, w.R, r["q_r"], w.T, path.read_slot,
+                                         path.kc[n], path.vc[n], lay.num_slots, path.out[n])
+
+    res = {}
+    for name, fused in (("separate_ms_per_layer", False), ("store_attend_ms_per_layer", True)):
+        run(fused)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            run(fused)
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / (reps * w.layers)
+    return res
 
 
 # ----------------------------------------------------------------------------- oracle
@@ -370,6 +418,87 @@ def cpu_oracle_sample(w, budget_s):
     return flops, t_total, cores, desc
 
 
+# ----------------------------------------------------------------------------- sweep
+def _per_launch_ms(fn, reps=5):
+    fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _launch_set(path):
+    """Per-launch times (ms) of one layer's probe, store and slot attention for the batch."""
+    ac, w, lay = path.ac, path.w, path.lay
+    p0, r0 = path.probe[0], path.rec[0]
+    probe = _per_launch_ms(lambda: ac.acache_probe_scores(
+        path.desc, w.batch, w.T, w.l, w.L, path.masked, w.m, p0["q"], p0["k_req"], p0["v_req"], p0["k_aff"],
+        p0["v_aff"], path.probe_out, path.scores, path.ws, path.ws_bytes))
+    write = _per_launch_ms(lambda: ac.acache_write_slots(
+        path.desc, w.batch, w.R, lay.private_slots, r0["k_new"], r0["v_new"], path.kc[0], path.vc[0],
+        lay.num_slots, lay.private_begin))
+    slot = _per_launch_ms(lambda: ac.acache_slot_attention(
+        path.desc, w.batch, w.R, r0["q_r"], w.T, path.read_slot, path.kc[0], path.vc[0], lay.num_slots,
+        path.out[0]))
+    return probe, write, slot
+
+
+def sweep(args):
+    """Per-launch measurements of the workloads other than the headline one.  Four layers are
+    materialised per workload (all layers have the same shapes, so a launch's time does not
+    depend on which layer it runs); whole-pass times are the per-launch times times the
+    launch counts and are labelled as such."""
+    peaks = measured_peaks()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak = peaks["bf16_tflops_sustained"]
+    for name, ratios in ((wl.DREAM_INFIX.name, (200,)), (wl.LLADA_PAGED.name, (200,)),
+                         (wl.LLADA_SUFFIX.name, (100, 200, 300))):
+        base = wl.CATALOGUE[name]
+        for ratio in ratios:
+            w = base.replace(layers=4, recompute_points=1, ratio_permille=ratio)
+            path = Path(w, dev)
+            path.step()
+            torch.cuda.synchronize()
+            probe_ms, write_ms, slot_ms = _launch_set(path)
+            row = w.hkv * w.d * w.esize
+            slot_tf = slot_flops_per_launch(w) / (slot_ms / 1e3) / 1e12
+            line = {"sweep": name, "ratio": ratio / 1000, "K": w.K, "R": w.R, "batch": w.batch, "T": w.T,
+                    "layers_full": base.layers, "recompute_points_full": base.recompute_points,
+                    "probe_ms_per_layer": probe_ms,
+                    "probe_tflops": probe_flops(w) / w.layers / (probe_ms / 1e3) / 1e12,
+                    "slot_attn_ms_per_launch": slot_ms, "slot_attn_tflops": slot_tf,
+                    "slot_attn_frac_of_peak": slot_tf / peak,
+                    "write_ms_per_launch": write_ms,
+                    "write_gbs": 4.0 * w.batch * w.R * row / (write_ms / 1e3) / 1e9,
+                    "anchor_scored_tokens_per_s_est": w.batch * w.L / (base.layers * probe_ms / 1e3),
+                    "full_pass_ms_est": base.layers * probe_ms + base.recompute_points * base.layers * (write_ms + slot_ms),
+                    "peak": {"bf16_tflops_sustained": peak, "hbm_gbs": peaks["hbm_gbs"], "source": peaks["source"]}}
+            if name == wl.LLADA_PAGED.name or (name == wl.DREAM_INFIX.name):
+                line["decode"] = Decode(path).measure(5, 2, peaks)
+            if name == wl.LLADA_SUFFIX.name and ratio == 200:
+                one = Path(w.replace(batch=1), dev)
+                one.step()
+                p1, _, _ = _launch_set(one)
+                line["probe_ms_per_request_batch1"] = base.layers * p1
+                del one
+                vs = {}
+                for b in (1, 2, 4, 8, 16, 32):
+                    pb = Path(w.replace(batch=b, layers=1), dev)
+                    pb.step()
+                    _, _, sb = _launch_set(pb)
+                    vs[b] = slot_flops_per_launch(pb.w) / (sb / 1e3) / 1e12
+                    del pb
+                line["slot_attn_tflops_vs_batch"] = vs
+            print(json.dumps(line), flush=True)
+            del path
+            torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------------------- main
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -412,6 +541,9 @@ def run_reference(args, w, world, rank):
 
 def main():
     args = parse()
+    if args.sweep:
+        sweep(args)
+        return
     w = wl.CATALOGUE[args.workload]
     if args.layers:
         w = w.replace(layers=args.layers)
@@ -485,6 +617,7 @@ def main():
     decode = None
     if not args.no_decode:
         decode = Decode(path).measure(max(args.steps, 5), 3, peaks)
+    fused = store_attend_compare(path)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -511,6 +644,8 @@ def main():
                          "peak": peak, "unit": "TFLOP/s", "frac": slot_achieved / peak,
                          "peak_source": f"{peaks['source']} bf16 sustained", "traffic": traffic},
             "decode": decode,
+            "store_then_attend": {"timing": "CUDA events, one recompute point over all layers, 3 passes",
+                                  **fused},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": path.launches_per_step * args.steps,
