@@ -183,8 +183,10 @@ class Path:
         self.launches_per_step = w.layers * 3 + 2 + w.recompute_points * w.layers * 2
         torch.cuda.synchronize()
 
-    def step(self, ev=None):
-        """One pass of the path.  `ev` (optional) collects CUDA events around phases."""
+    def step(self, ev=None, e2e=False):
+        """One pass of the path.  `ev` (optional) collects CUDA events around phases; with
+        `e2e` the step waits for each layer's uploaded inputs and records when it is done
+        with them (see step_e2e)."""
         ac, w, lay = self.ac, self.w, self.lay
         s = torch.cuda.current_stream()
         self.scores.zero_()
@@ -193,9 +195,13 @@ class Path:
             e0.record(s)
         for n in range(w.layers):
             p = self.probe[n]
+            if e2e:
+                s.wait_event(self.ev_probe_ready[n])
             ac.acache_probe_scores(self.desc, w.batch, w.T, w.l, w.L, self.masked, w.m, p["q"],
                                    p["k_req"], p["v_req"], p["k_aff"], p["v_aff"], self.probe_out,
                                    self.scores, self.ws, self.ws_bytes)
+            if e2e:
+                self.ev_probe_done[n].record(s)
         ac.acache_topk_anchors(self.scores, w.batch, w.L, w.K, self.anchors)
         if ev is not None:
             e1 = torch.cuda.Event(enable_timing=True)
@@ -203,9 +209,11 @@ class Path:
             ev["select"].append((e0, e1))
         ac.acache_build_slot_maps(w.batch, w.T, w.l, w.L, w.K, self.anchors, lay.shared_slot,
                                   lay.private_slots, self.write_pos, self.read_slot)
-        for _ in range(w.recompute_points):
+        for point in range(w.recompute_points):
             for n in range(w.layers):
                 r = self.rec[n]
+                if e2e and point == 0:
+                    s.wait_event(self.ev_rec_ready[n])
                 ac.acache_write_slots(self.desc, w.batch, w.R, lay.private_slots, r["k_new"],
                                       r["v_new"], self.kc[n], self.vc[n], lay.num_slots,
                                       lay.private_begin)
@@ -218,6 +226,8 @@ class Path:
                     b = torch.cuda.Event(enable_timing=True)
                     b.record(s)
                     ev["slot"].append((a, b))
+                if e2e and point == w.recompute_points - 1:
+                    self.ev_rec_done[n].record(s)
 
     # ---- host buffers for the end-to-end measurement ---------------------------------
     def host_inputs(self):
@@ -231,18 +241,42 @@ class Path:
         bi = sum(t.numel() * t.element_size() for p in self.h_probe for t in p.values())
         bi += sum(t.numel() * t.element_size() for r in self.h_rec for t in r.values())
         bo = sum(t.numel() * t.element_size() for t in (self.h_anchors, self.h_scores, self.h_out))
+        self.copy_stream = torch.cuda.Stream()
+        L = self.w.layers
+        self.ev_probe_done = [torch.cuda.Event() for _ in range(L)]
+        self.ev_probe_ready = [torch.cuda.Event() for _ in range(L)]
+        self.ev_rec_done = [torch.cuda.Event() for _ in range(L)]
+        self.ev_rec_ready = [torch.cuda.Event() for _ in range(L)]
+        for e in self.ev_probe_done + self.ev_rec_done:   # nothing to wait for before the first step
+            e.record()
         return bi, bo
 
     def step_e2e(self):
-        for n in range(self.w.layers):
-            for k, v in self.h_probe[n].items():
-                self.probe[n][k].copy_(v, non_blocking=True)
-            for k, v in self.h_rec[n].items():
-                self.rec[n][k].copy_(v, non_blocking=True)
-        self.step()
+        """One step end to end: every input of the step is copied from pinned host memory and
+        the step's results (scores, anchors, the last layer's attention output) are read
+        back.  The copies run on their own stream, layer by layer, gated by events, so the
+        next step's inputs upload while the current step computes: a layer's probe inputs as
+        soon as its probe has run, its recompute inputs once the last recompute point has
+        read them."""
+        w, s = self.w, torch.cuda.current_stream()
+        cs = self.copy_stream
+        for n in range(w.layers):
+            cs.wait_event(self.ev_probe_done[n])
+            with torch.cuda.stream(cs):
+                for k, v in self.h_probe[n].items():
+                    self.probe[n][k].copy_(v, non_blocking=True)
+            self.ev_probe_ready[n].record(cs)
+        for n in range(w.layers):
+            cs.wait_event(self.ev_rec_done[n])
+            with torch.cuda.stream(cs):
+                for k, v in self.h_rec[n].items():
+                    self.rec[n][k].copy_(v, non_blocking=True)
+            self.ev_rec_ready[n].record(cs)
+        self.step(e2e=True)
         self.h_anchors.copy_(self.anchors, non_blocking=True)
         self.h_scores.copy_(self.scores, non_blocking=True)
         self.h_out.copy_(self.out[-1], non_blocking=True)
+        s.wait_stream(cs)
 
 
 class Decode:
@@ -603,6 +637,7 @@ def main():
         barrier()
         e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_s.record()
+        path.copy_stream.wait_event(e_s)
         n_e2e = max(1, min(args.steps, 5))
         for _ in range(n_e2e):
             path.step_e2e()
