@@ -29,9 +29,11 @@
 // tc_colsum_kernel  (second probe pass: masked-to-affix attention mass; one CTA per
 //                    (request, query head, 128 affix keys))
 //   D = K_affix_tile Q_masked_chunk^T (SS MMA, M = 128 affix keys, N = 128 masked rows);
-//   masked query rows are gathered with `tile::gather4`; thread r owns affix key r and sums
-//   2^(logit - m_k) / l_k over the masked rows k in ascending order -- a per-thread serial
-//   sum, so the result is deterministic and no cross-thread reduction is needed.
+//   a chunk of masked query rows that are consecutive probe rows (the usual case: the
+//   generation positions) is two tiled box loads, other chunks are gathered with
+//   `tile::gather4`; thread r owns affix key r and sums 2^(logit - m_k) / l_k over the masked
+//   rows k into four partial sums in a fixed order -- a per-thread sum, so the result is
+//   deterministic and no cross-thread reduction is needed.
 //
 // Every mbarrier wait is bounded (about a second); a wait that gives up raises a CTA-wide
 // abort flag and ACACHE_DEV_TIMEOUT, every role leaves its loop, in-flight MMAs are drained
@@ -551,6 +553,7 @@ constexpr uint32_t kCsTmemCols = 256;
 struct ColsumParams {
     CUtensorMap tm_kaff;  // 3-D affix keys [L][Hkv][d], box {64, 1, 128}
     CUtensorMap tm_q;     // 2-D probe queries [B*P*Hq][d], box {64, 1} (gather4)
+    CUtensorMap tm_qbox;  // 4-D probe queries [B][P][Hq][d], box {64, 1, 128, 1}
     const int32_t* masked;
     const float* stat_m;
     const float* stat_l;
@@ -573,7 +576,7 @@ struct ColsumCtl {
     float st_il[kCsStages][kBN];      // 1 / row sum; 0 = skip
 };
 
-__global__ void __launch_bounds__(kCsThreads, 1)
+__global__ void __launch_bounds__(kCsThreads, 2)
 tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     extern __shared__ uint8_t dsm[];
     __shared__ ColsumCtl ctl;
@@ -654,11 +657,30 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
                 ctl.st_m[s][4 * lane + u] = sm[u];
                 ctl.st_il[s][4 * lane + u] = sil[u];
             }
+            // The initially masked rows are normally one run of consecutive probe rows (the
+            // generation positions): then the chunk is two tiled box loads of 128 rows instead
+            // of 64 gathers.  Rows of the box past the masked set are loaded but skipped (their
+            // statistics say so); rows past P read as zeros.
+            const int r0 = __shfl_sync(0xffffffffu, mrow[min(c * kBN, p.m - 1)], 0);
+            bool run = r0 >= 0 && r0 + kBN <= p.P + kBN;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = c * kBN + 4 * lane + u;
+                if (k < p.m) run = run && mrow[k] == r0 + 4 * lane + u;
+            }
+            run = __all_sync(0xffffffffu, run);
             if (lane == 0) mbar_arrive_expect_tx(&ctl.b_full[s], kTileBytes);
             __syncwarp();
-            const uint32_t o = (uint32_t)lane * 512u;
-            tma_gather4(sB + o, &p.tm_q, 0, rows[0], rows[1], rows[2], rows[3], &ctl.b_full[s]);
-            tma_gather4(sB + kRegion + o, &p.tm_q, 64, rows[0], rows[1], rows[2], rows[3], &ctl.b_full[s]);
+            if (run) {
+                if (lane == 0) {
+                    tma_load_4d(sB, &p.tm_qbox, 0, h, r0, b, &ctl.b_full[s]);
+                    tma_load_4d(sB + kRegion, &p.tm_qbox, 64, h, r0, b, &ctl.b_full[s]);
+                }
+            } else {
+                const uint32_t o = (uint32_t)lane * 512u;
+                tma_gather4(sB + o, &p.tm_q, 0, rows[0], rows[1], rows[2], rows[3], &ctl.b_full[s]);
+                tma_gather4(sB + kRegion + o, &p.tm_q, 64, rows[0], rows[1], rows[2], rows[3], &ctl.b_full[s]);
+            }
             if (lane != 0) mbar_arrive(&ctl.b_full[s]);
         }
     } else if (warp == kCsMmaWarp) {
@@ -689,7 +711,9 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
         const int r = threadIdx.x;                         // affix key j0 + r
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const float c2 = p.scale_log2;
-        float acc = 0.f;
+        // four partial sums (masked row k goes to sum k % 4), added in a fixed order at the
+        // end: deterministic, and four times shorter dependency chains
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
         for (int c = 0; c < n_ch; ++c) {
             const int s = c % kCsStages, db = c & 1;
@@ -707,13 +731,15 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int k = cc * 32 + i;
-                    acc += fast_exp2(fmaf(__uint_as_float(v[i]), c2, -ctl.st_m[s][k])) * ctl.st_il[s][k];
+                    acc4[i & 3] = fmaf(fast_exp2(fmaf(__uint_as_float(v[i]), c2, -ctl.st_m[s][k])), ctl.st_il[s][k],
+                                       acc4[i & 3]);
                 }
             }
             tc_fence_before();
             mbar_arrive(&ctl.cons_done[db]);
         }
-        if (ok && j0 + r < p.L) p.partial[((int64_t)b * p.Hq + h) * p.L + j0 + r] = acc;
+        if (ok && j0 + r < p.L)
+            p.partial[((int64_t)b * p.Hq + h) * p.L + j0 + r] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
     }
     tc_fence_before();
     __syncthreads();
@@ -859,7 +885,9 @@ int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int
     ColsumParams prm{};
     const uint64_t da[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)L};
     const uint64_t dq[2] = {(uint64_t)kD, (uint64_t)B * P * a.hq};
-    if (!make_map(&prm.tm_kaff, k_aff, 3, da, 2, kBN) || !make_map(&prm.tm_q, q, 2, dq, 1, 1))
+    const uint64_t dqb[4] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)P, (uint64_t)B};
+    if (!make_map(&prm.tm_kaff, k_aff, 3, da, 2, kBN) || !make_map(&prm.tm_q, q, 2, dq, 1, 1) ||
+        !make_map(&prm.tm_qbox, q, 4, dqb, 2, kBN))
         return ACACHE_ERR_CUDA;
     prm.masked = masked_rows;
     prm.stat_m = stat_m;
