@@ -216,6 +216,12 @@ ACACHE_DEVFN void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" :
 // Let the next grid on the stream start its prologue before this grid has finished.
 ACACHE_DEVFN void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Named barrier `id` (1-15; 0 is the one __syncthreads uses) over `count` threads, a multiple
+// of 32: whole warps of a subset of the CTA synchronise without involving the other warps.
+ACACHE_DEVFN void named_barrier_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---- thread-block clusters (distributed shared memory) ------------------------------------
 ACACHE_DEVFN uint32_t cluster_ctarank() {
     uint32_t r;

@@ -18,13 +18,22 @@
 //   WG2       warp 8 allocates TMEM (S_A, S_B, O_A, O_B: 128 fp32 columns each); lane 0 of
 //             warp 8 issues tile A's MMAs, lane 0 of warp 9 tile B's:
 //             S_t(j) = Q_t K_j^T (SS, M = N = 128) and O_t += P_t(j) V_j (TS: P from TMEM,
-//             V an MN-major shared-memory operand), S_t(j+1) right after PV_t(j).
-//   WG3       TMA producers: warps 12-13 fill a 3-stage K ring, warps 14-15 a 2-stage V ring.
-//             Read-slot keys: each lane issues one `tile::gather4` per tile (4 pool rows x 64
-//             columns, rows resolved through the read-slot map one tile ahead).  Probe keys:
-//             the affix rows and the request's own rows are contiguous per KV head, so a tile
-//             is two tiled box loads.  Loads complete on the stage's mbarrier by byte count.
+//             V an MN-major shared-memory operand), S_t(j+1) right after PV_t(j).  Warps 10
+//             and 11 are TMA producers.
+//   WG3       TMA producers: warps 12, 13 and 10 fill a 3-stage K ring, warps 14, 15 and 11 a
+//             2-stage V ring.  Read-slot keys: a tile is 64 `tile::gather4` loads (4 pool rows
+//             x 64 columns, rows resolved through the read-slot map one tile ahead), about 21
+//             per warp -- each gather4 a lane issues costs its warp tens of cycles, so the
+//             gather rate grows with the number of issuing warps.  Probe keys: the affix rows
+//             and the request's own rows are contiguous per KV head, so a tile is two tiled
+//             box loads.  Loads complete on the stage's mbarrier by byte count.
 //   setmaxnreg gives the softmax warpgroups 200 registers and WG2 / WG3 56.
+//   A CTA left with one Q tile (the ragged last query block) splits its keys instead: chain A
+//   takes the first half of the key tiles and chain B the second half, both against the same
+//   Q tile, so the two chains still ping-pong; the K/V rings then alternate A's and B's tiles,
+//   the free Q buffer becomes a third V stage, and at the end chain B hands its row maximum
+//   and row sum to chain A through shared memory, which merges the two partial softmax states
+//   (O_A 2^(m_A-m) + O_B 2^(m_B-m), likewise the sums) before the epilogue.
 //
 // tc_colsum_kernel  (second probe pass: masked-to-affix attention mass; one CTA per
 //                    (request, query head, 128 affix keys))
@@ -58,16 +67,14 @@ constexpr int kKStages = 3;                 // K ring: a K tile is free once S_B
 constexpr int kVStages = 2;                 // V ring: a V tile is free once PV_B has read it
 constexpr int kMmaWarp = 8;                 // warpgroup 2: TMEM allocation; warps 8 and 9 each
                                             // issue the MMAs of one Q tile
-constexpr int kProdWarp = 12;               // warpgroup 3: the 4 TMA producer warps
-constexpr int kProdWarps = 4;               // one per SM sub-partition: gather4 issue runs in
-                                            // parallel on the four of them
+constexpr int kProdWarp = 12;               // warpgroup 3: TMA producer warps (joined by the
+constexpr int kProdWarps = 4;               // idle warps 10 and 11 of warpgroup 2)
 constexpr int kThreads = 16 * 32;
+static_assert(kThreads == (kProdWarp + kProdWarps) * 32, "warp roles");
 // Registers: 512 threads x 128 at launch = 65536; the softmax warpgroups grow to 200, the
 // MMA / producer warpgroups shrink to 56: 2*128*200 + 2*128*56 = 65536.
 constexpr int kRegSoftmax = 200, kRegOther = 56;
 static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther <= kThreads * 128, "register split");
-constexpr int kGathersPerWarp = 4 * (kBN / 4) / kProdWarps;   // 32: one gather4 per lane
-                                                               // (warps 12-13: K, 14-15: V)
 constexpr uint32_t kTileBytes = kBN * kD * 2;     // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t kRegion = kBN * 128;           // 16 KB: 64 columns of a 128-row tile
 constexpr uint32_t kSmemBytes = kTileBytes * (kQT + kKStages + kVStages) + 1024;
@@ -101,8 +108,8 @@ struct AttnCtl {
     uint64_t q_full;
     uint64_t k_full[kKStages];
     uint64_t k_empty[kKStages];
-    uint64_t v_full[kVStages];
-    uint64_t v_empty[kVStages];
+    uint64_t v_full[kVStages + 1];    // + the stage in the free Q buffer (split keys)
+    uint64_t v_empty[kVStages + 1];
     uint64_t s_full[kQT];
     uint64_t p_half[kQT];   // first half of P_t(j) (keys 0-63) is in TMEM
     uint64_t p_full[kQT];   // all of P_t(j) is in TMEM
@@ -110,6 +117,32 @@ struct AttnCtl {
     uint64_t turn[kQT];     // softmax ping-pong: turn[t] completes when tile t may exponentiate
     uint32_t tmem_base;
     int abort;
+    int split_ok;           // split keys: chain B's partial state below is complete
+    float split_m[kBM];     //   chain B's row maximum (the exponent offset it used) and row sum
+    float split_l[kBM];
+};
+
+// Key-tile schedule of a CTA.  Ring entry e is the e-th K/V tile the producers load; chain t
+// reads its i-th key tile from entry entry(t, i).  Unsplit: every chain reads every key tile
+// and entry e holds tile e.  Split (one Q tile): chain 0 reads tiles [0, n0), chain 1 tiles
+// [n0, n_kv); entries alternate chain 0, chain 1, ..., and the last tile of chain 0 (odd
+// n_kv) is the last entry.
+struct KeySchedule {
+    bool split;
+    int n_kv, n0;
+    ACACHE_DEVFN int n_tiles(int t) const { return split ? (t == 0 ? n0 : n_kv - n0) : n_kv; }
+    ACACHE_DEVFN int tile(int t, int i) const { return (split && t == 1) ? n0 + i : i; }
+    ACACHE_DEVFN int entry(int t, int i) const {
+        if (!split) return i;
+        const int n1 = n_kv - n0;
+        return i < n1 ? 2 * i + t : n1 + i;
+    }
+    ACACHE_DEVFN int entry_tile(int e) const {
+        if (!split) return e;
+        const int n1 = n_kv - n0;
+        if (e < 2 * n1) return (e & 1) ? n0 + (e >> 1) : (e >> 1);
+        return e - n1;
+    }
 };
 
 // Bounded wait that also leaves early once another role has aborted.
@@ -183,20 +216,29 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     if (q0 >= n_rows) return;
     const int n_qt = min(kQT, (n_rows - q0 + kBM - 1) / kBM);   // Q tiles present (1 or 2)
     const int n_kv = n_key_tiles<kMode>(p, T_len);
+    // one Q tile and at least two key tiles: split the keys between the two chains
+    const bool split = n_qt == 1 && n_kv >= 2;
+    const int n_ch = split ? 2 : n_qt;                  // chains: softmax warpgroups, MMA threads
+    const KeySchedule ks{split, n_kv, split ? (n_kv + 1) / 2 : n_kv};
+    // with split keys the second Q buffer is free and serves as a third V stage
+    const int n_vst = split ? kVStages + 1 : kVStages;
+    auto sVs = [&](int s) { return s < kVStages ? sV(s) : sQ(1); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 1);
-        // a K or V stage is free once the MMA thread of every present Q tile is done with it
+        // a K or V stage is free once every chain that reads its entry is done with it (both
+        // Q tiles' chains; with split keys the one chain the entry belongs to)
+        const int readers = split ? 1 : n_qt;
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&ctl.k_full[s], 1);
-            mbar_init(&ctl.k_empty[s], n_qt);
+            mbar_init(&ctl.k_empty[s], readers);
         }
-        for (int s = 0; s < kVStages; ++s) {
+        for (int s = 0; s < kVStages + 1; ++s) {
             mbar_init(&ctl.v_full[s], 1);
-            mbar_init(&ctl.v_empty[s], n_qt);
+            mbar_init(&ctl.v_empty[s], readers);
         }
         for (int t = 0; t < kQT; ++t) {
             mbar_init(&ctl.s_full[t], 1);
@@ -206,6 +248,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             mbar_init(&ctl.turn[t], 128);
         }
         ctl.abort = 0;
+        ctl.split_ok = 1;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -219,175 +262,185 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
 
     // Each role's code sits inside the branch of its register reallocation, so the compiler
     // allocates every region against the right register limit.
-    if (wg == 3) {
-        // ------------------------------------------------------------------ TMA producers
+    if (wg >= 2) {
         setmaxnreg_dec<kRegOther>();
-        const int pw = warp - kProdWarp;
-        if (pw == 0 && lane == 0) {
-            tma_prefetch_desc(&p.tm_q);
-            tma_prefetch_desc(&p.tm_k0);
-            tma_prefetch_desc(&p.tm_v0);
-            if (kMode == kProbeKeys) {
-                tma_prefetch_desc(&p.tm_k1);
-                tma_prefetch_desc(&p.tm_v1);
-            }
-            mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_qt);
-            for (int t = 0; t < n_qt; ++t) {
-                if (kMode == kSlotKeys && p.q_start) {   // 3-D map over the flattened rows
-                    const int r = (int)(qbase + q0 + t * kBM);
-                    tma_load_3d(sQ(t), &p.tm_q, 0, h, r, &ctl.q_full);
-                    tma_load_3d(sQ(t) + kRegion, &p.tm_q, 64, h, r, &ctl.q_full);
-                } else {
-                    tma_load_4d(sQ(t), &p.tm_q, 0, h, q0 + t * kBM, b, &ctl.q_full);
-                    tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, h, q0 + t * kBM, b, &ctl.q_full);
+        if (warp >= kMmaWarp + 2) {
+            // -------------------------------------------------------------- TMA producers
+            if (warp == kProdWarp && lane == 0) {
+                tma_prefetch_desc(&p.tm_q);
+                tma_prefetch_desc(&p.tm_k0);
+                tma_prefetch_desc(&p.tm_v0);
+                if (kMode == kProbeKeys) {
+                    tma_prefetch_desc(&p.tm_k1);
+                    tma_prefetch_desc(&p.tm_v1);
                 }
-            }
-        }
-        // warps 12-13 fill the K ring, warps 14-15 the V ring; probe tiles are box loads
-        // issued by lane 0 of warps 12 (K) and 14 (V)
-        const bool is_v = pw >= 2;
-        const int nst = is_v ? kVStages : kKStages;
-        uint64_t* full = is_v ? ctl.v_full : ctl.k_full;
-        uint64_t* empty = is_v ? ctl.v_empty : ctl.k_empty;
-        const CUtensorMap* tm_aff = is_v ? &p.tm_v0 : &p.tm_k0;   // slot: the pool
-        const CUtensorMap* tm_own = is_v ? &p.tm_v1 : &p.tm_k1;
-        const bool leader = (pw & 1) == 0 && lane == 0;            // announces the tile's bytes
-        if (kMode == kSlotKeys || (pw & 1) == 0) {
-            const int n_aff = (p.L + kBN - 1) / kBN;
-            const int oob_row = (int)(p.num_slots * p.Hkv);     // first row outside the pool
-            // read-slot keys: this lane's gather x = 4-row group x / 2 of the tile, column
-            // half x % 2 of the warp pair's matrix (K or V)
-            const int x = (pw & 1) * 32 + lane;
-            const int g = x >> 1, half = x & 1;
-            // rows of tile j are resolved one iteration ahead, so the read-slot loads overlap
-            // the previous tile's wait and gather issue
-            auto resolve = [&](int j, int (&rows)[4]) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int t = j * kBN + 4 * g + u;
-                    rows[u] = oob_row;
-                    if (kMode == kSlotKeys && j < n_kv && t < T_len) {
-                        const int64_t slot = p.read_slot[kbase + t];
-                        if (slot >= 0 && slot < p.num_slots)
-                            rows[u] = (int)(slot * p.Hkv + hk);
-                        else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
-                            flag(dev_status, ACACHE_DEV_BAD_SLOT);
-                    }
-                }
-            };
-            int next[4];
-            resolve(0, next);
-            // store-then-attend: the pool rows this launch reads may have been written by the
-            // preceding store grid (launched ahead with programmatic stream serialisation)
-            grid_dependency_wait();
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % nst;
-                const uint32_t dst_tile = is_v ? sV(s) : sK(s);
-                int rows[4] = {next[0], next[1], next[2], next[3]};
-                resolve(j + 1, next);
-                if (j >= nst &&
-                    !__all_sync(0xffffffffu, wait_bar(&empty[s], ((j / nst) - 1) & 1, abort_flag,
-                                                      dev_status)))
-                    break;
-                // the warp pair's first warp announces the tile's bytes; a gather of the other
-                // warp that completes first leaves the count transiently negative (allowed)
-                if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
-                __syncwarp();
-                if (kMode == kSlotKeys) {
-                    tma_gather4(dst_tile + (uint32_t)half * kRegion + (uint32_t)g * 512u, tm_aff, half * 64,
-                                rows[0], rows[1], rows[2], rows[3], &full[s]);
-                } else if (lane == 0) {
-                    if (j < n_aff) {
-                        const int j0 = j * kBN;
-                        tma_load_3d(dst_tile, tm_aff, 0, hk, j0, &full[s]);
-                        tma_load_3d(dst_tile + kRegion, tm_aff, 64, hk, j0, &full[s]);
+                mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_qt);
+                for (int t = 0; t < n_qt; ++t) {
+                    if (kMode == kSlotKeys && p.q_start) {   // 3-D map over the flattened rows
+                        const int r = (int)(qbase + q0 + t * kBM);
+                        tma_load_3d(sQ(t), &p.tm_q, 0, h, r, &ctl.q_full);
+                        tma_load_3d(sQ(t) + kRegion, &p.tm_q, 64, h, r, &ctl.q_full);
                     } else {
-                        const int r0 = (j - n_aff) * kBN;
-                        tma_load_4d(dst_tile, tm_own, 0, hk, r0, b, &full[s]);
-                        tma_load_4d(dst_tile + kRegion, tm_own, 64, hk, r0, b, &full[s]);
+                        tma_load_4d(sQ(t), &p.tm_q, 0, h, q0 + t * kBM, b, &ctl.q_full);
+                        tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, h, q0 + t * kBM, b, &ctl.q_full);
                     }
                 }
             }
-        }
-    } else if (wg == 2) {
-        setmaxnreg_dec<kRegOther>();
-        // ------------------------------------------------------------------ MMA issuers
-        // Warp 8 issues the MMAs of Q tile A, warp 9 those of tile B, so the two chains never
-        // wait on each other and their issue runs on two SM sub-partitions.  Per key tile j a
-        // thread issues PV_t(j) once P_t(j) is in TMEM, then S_t(j+1).  tcgen05 MMAs of one
-        // thread run in issue order, so S_t(j+1) may overwrite the columns P_t(j) occupies,
-        // and the completion of S_t(j) implies that of PV_t(j-1).
-        const int t = warp - kMmaWarp;
-        if (t < n_qt && lane == 0) {
-            const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-            const uint32_t idO = idesc_bf16(kBM, kD, false, true);
-            const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
-            const uint64_t dq = sdesc_sw128(sQ(t), 16, 1024);
-            // descriptor start addresses advance in 16-byte units: K step k of a K-major tile
-            // is 32 bytes into region k / 4; of the MN-major V tile, 16 rows (2048 bytes)
-            auto issue_s = [&](int j) {
-                const uint64_t dk = sdesc_sw128(sK(j % kKStages), 16, 1024);
+            // warps 12, 13 and 10 fill the K ring, warps 14, 15 and 11 the V ring (a gather4 costs
+            // its warp tens of cycles of issue, so the tile's 64 are spread over three warps); probe
+            // tiles are box loads issued by lane 0 of warps 12 (K) and 14 (V)
+            const bool is_v = warp == kMmaWarp + 3 || warp >= kProdWarp + 2;
+            const int pi = warp >= kProdWarp ? (warp - kProdWarp) & 1 : 2;   // place in the ring's trio
+            const int nst = is_v ? n_vst : kKStages;
+            uint64_t* full = is_v ? ctl.v_full : ctl.k_full;
+            uint64_t* empty = is_v ? ctl.v_empty : ctl.k_empty;
+            const CUtensorMap* tm_aff = is_v ? &p.tm_v0 : &p.tm_k0;   // slot: the pool
+            const CUtensorMap* tm_own = is_v ? &p.tm_v1 : &p.tm_k1;
+            const bool leader = pi == 0 && lane == 0;                  // announces the tile's bytes
+            if (kMode == kSlotKeys || pi == 0) {
+                const int n_aff = (p.L + kBN - 1) / kBN;
+                const int oob_row = (int)(p.num_slots * p.Hkv);     // first row outside the pool
+                // read-slot keys: this lane's gather x = 4-row group x / 2 of the tile, column
+                // half x % 2 of the trio's matrix (K or V); lanes with x >= 64 have none
+                const int x = 3 * lane + pi;
+                const bool gathers = x < 64;
+                const int g = x >> 1, half = x & 1;
+                // rows of tile j are resolved one iteration ahead, so the read-slot loads overlap
+                // the previous tile's wait and gather issue
+                auto resolve = [&](int j, int (&rows)[4]) {
 #pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint64_t ko = ((uint64_t)(k >> 2) * kRegion + (uint64_t)(k & 3) * 32u) >> 4;
-                    umma_ss(d_s, dq + ko, dk + ko, idS, k > 0);
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = j * kBN + 4 * g + u;
+                        rows[u] = oob_row;
+                        if (kMode == kSlotKeys && gathers && j < n_kv && t < T_len) {
+                            const int64_t slot = p.read_slot[kbase + t];
+                            if (slot >= 0 && slot < p.num_slots)
+                                rows[u] = (int)(slot * p.Hkv + hk);
+                            else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
+                                flag(dev_status, ACACHE_DEV_BAD_SLOT);
+                        }
+                    }
+                };
+                int next[4];
+                resolve(ks.entry_tile(0), next);
+                // store-then-attend: the pool rows this launch reads may have been written by the
+                // preceding store grid (launched ahead with programmatic stream serialisation)
+                grid_dependency_wait();
+                for (int e = 0; e < n_kv; ++e) {          // ring entries in load order
+                    const int s = e % nst;
+                    const int j = ks.entry_tile(e);           // the key tile entry e holds
+                    const uint32_t dst_tile = is_v ? sVs(s) : sK(s);
+                    int rows[4] = {next[0], next[1], next[2], next[3]};
+                    resolve(e + 1 < n_kv ? ks.entry_tile(e + 1) : n_kv, next);
+                    if (e >= nst &&
+                        !__all_sync(0xffffffffu, wait_bar(&empty[s], ((e / nst) - 1) & 1, abort_flag,
+                                                          dev_status)))
+                        break;
+                    // the trio's first warp announces the tile's bytes; a gather of another warp
+                    // that completes first leaves the count transiently negative (allowed)
+                    if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
+                    __syncwarp();
+                    if (kMode == kSlotKeys) {
+                        if (gathers)
+                            tma_gather4(dst_tile + (uint32_t)half * kRegion + (uint32_t)g * 512u, tm_aff, half * 64,
+                                        rows[0], rows[1], rows[2], rows[3], &full[s]);
+                    } else if (lane == 0) {
+                        if (j < n_aff) {
+                            const int j0 = j * kBN;
+                            tma_load_3d(dst_tile, tm_aff, 0, hk, j0, &full[s]);
+                            tma_load_3d(dst_tile + kRegion, tm_aff, 64, hk, j0, &full[s]);
+                        } else {
+                            const int r0 = (j - n_aff) * kBN;
+                            tma_load_4d(dst_tile, tm_own, 0, hk, r0, b, &full[s]);
+                            tma_load_4d(dst_tile + kRegion, tm_own, 64, hk, r0, b, &full[s]);
+                        }
+                    }
                 }
-                umma_commit(&ctl.s_full[t]);
-                umma_commit(&ctl.k_empty[j % kKStages]);
-            };
-            // PV_t(j) in two halves of the key tile: keys 0-63 (k steps 0-3) as soon as the
-            // softmax has published the first half of P, keys 64-127 once all of P is in
-            auto issue_pv_half = [&](int j, int h) {
-                const uint64_t dv = sdesc_sw128(sV(j % kVStages), kRegion, 1024);
-#pragma unroll
-                for (int k = 4 * h; k < 4 * h + 4; ++k)
-                    umma_ts(d_o, d_s + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (j > 0 || k > 0));
-            };
-            bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status) &&
-                      wait_bar(&ctl.k_full[0], 0, abort_flag, dev_status);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                ok = wait_bar(&ctl.v_full[j % kVStages], (j / kVStages) & 1, abort_flag, dev_status) &&
-                     wait_bar(&ctl.p_half[t], j & 1, abort_flag, dev_status);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_half(j, 0);
-                ok = wait_bar(&ctl.p_full[t], j & 1, abort_flag, dev_status);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_half(j, 1);
-                umma_commit(&ctl.v_empty[j % kVStages]);
-                if (j + 1 < n_kv) {
-                    ok = wait_bar(&ctl.k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
-                                  abort_flag, dev_status);
+        } else {
+            // ------------------------------------------------------------------ MMA issuers
+            // Warp 8 issues the MMAs of Q tile A, warp 9 those of tile B, so the two chains never
+            // wait on each other and their issue runs on two SM sub-partitions.  Per key tile j a
+            // thread issues PV_t(j) once P_t(j) is in TMEM, then S_t(j+1).  tcgen05 MMAs of one
+            // thread run in issue order, so S_t(j+1) may overwrite the columns P_t(j) occupies,
+            // and the completion of S_t(j) implies that of PV_t(j-1).
+            const int t = warp - kMmaWarp;
+            if (t < n_ch && lane == 0) {
+                const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+                const uint32_t idO = idesc_bf16(kBM, kD, false, true);
+                const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
+                const uint64_t dq = sdesc_sw128(sQ(split ? 0 : t), 16, 1024);
+                const int nt = ks.n_tiles(t);
+                // descriptor start addresses advance in 16-byte units: K step k of a K-major tile
+                // is 32 bytes into region k / 4; of the MN-major V tile, 16 rows (2048 bytes)
+                auto issue_s = [&](int e) {                   // e: ring entry of the K tile
+                    const uint64_t dk = sdesc_sw128(sK(e % kKStages), 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const uint64_t ko = ((uint64_t)(k >> 2) * kRegion + (uint64_t)(k & 3) * 32u) >> 4;
+                        umma_ss(d_s, dq + ko, dk + ko, idS, k > 0);
+                    }
+                    umma_commit(&ctl.s_full[t]);
+                    umma_commit(&ctl.k_empty[e % kKStages]);
+                };
+                // PV_t(i) in two halves of the key tile: keys 0-63 (k steps 0-3) as soon as the
+                // softmax has published the first half of P, keys 64-127 once all of P is in
+                auto issue_pv_half = [&](int e, bool acc, int h) {
+                    const uint64_t dv = sdesc_sw128(sVs(e % n_vst), kRegion, 1024);
+#pragma unroll
+                    for (int k = 4 * h; k < 4 * h + 4; ++k)
+                        umma_ts(d_o, d_s + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (acc || k > 0));
+                };
+                const int e0 = ks.entry(t, 0);
+                bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status) &&
+                          wait_bar(&ctl.k_full[e0 % kKStages], (e0 / kKStages) & 1, abort_flag, dev_status);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(e0);
+                }
+                for (int i = 0; ok && i < nt; ++i) {
+                    const int e = ks.entry(t, i);
+                    ok = wait_bar(&ctl.v_full[e % n_vst], (e / n_vst) & 1, abort_flag, dev_status) &&
+                         wait_bar(&ctl.p_half[t], i & 1, abort_flag, dev_status);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(j + 1);
+                    issue_pv_half(e, i > 0, 0);
+                    ok = wait_bar(&ctl.p_full[t], i & 1, abort_flag, dev_status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv_half(e, i > 0, 1);
+                    umma_commit(&ctl.v_empty[e % n_vst]);
+                    if (i + 1 < nt) {
+                        const int en = ks.entry(t, i + 1);
+                        ok = wait_bar(&ctl.k_full[en % kKStages], (en / kKStages) & 1, abort_flag, dev_status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(en);
+                    }
                 }
+                // no MMA may still run when TMEM is released
+                umma_commit(&ctl.drain[t]);
+                mbar_wait(&ctl.drain[t], 0, kBudget);
             }
-            // no MMA may still run when TMEM is released
-            umma_commit(&ctl.drain[t]);
-            mbar_wait(&ctl.drain[t], 0, kBudget);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         setmaxnreg_inc<kRegSoftmax>();
-        if (wg < n_qt) {
+        if (wg < n_ch) {
         // ------------------------------------------------------------------ softmax + epilogue
-        const int t = wg;                                  // Q tile of this warpgroup
+        const int t = wg;                                  // chain (Q tile) of this warpgroup
         const int r = threadIdx.x - t * 128;               // query row in the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float c = p.scale_log2;                      // > 0
         // With two Q tiles the warpgroups take turns: A(0), B(0), A(1), B(1), ...  Each then
         // has the SM's issue slots and exponential units to itself, and the tensor core runs
         // one tile's MMAs while the other tile's softmax runs, instead of both at once.
-        const bool pingpong = n_qt > 1;
+        const bool pingpong = n_ch > 1;
+        const int nt = ks.n_tiles(t);
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
+        for (int i = 0; i < nt; ++i) {
+            const int j = ks.tile(t, i);                   // key tile of this step
             // discarded keys of tile j: bit i of drop[cc] = key 32 cc + i (loaded before the
             // wait for S_t(j), which hides the latency)
             uint32_t drop[4] = {0u, 0u, 0u, 0u};
@@ -399,7 +452,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     drop[cc] = __ballot_sync(0xffffffffu, tk < T_len && rs[tk] == ACACHE_SLOT_NONE);
                 }
             }
-            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], j & 1, abort_flag, dev_status));
+            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], i & 1, abort_flag, dev_status));
             if (!ok) break;
             tc_fence_after();
             // S_t(j) is read into registers as soon as it is ready -- typically while the tensor
@@ -409,8 +462,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_base + col_s(t) + cc * 32, v[cc]);
             tmem_ld_wait();
-            if (pingpong && (t == 1 || j > 0))
-                ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], (t == 0 ? j - 1 : j) & 1,
+            if (pingpong && (t == 1 || i > 0))
+                ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], (t == 0 ? i - 1 : i) & 1,
                                                       abort_flag, dev_status));
             if (!ok) break;
             const int valid = tile_valid<kMode>(p, j, T_len);
@@ -443,7 +496,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
             float alpha = 1.f;
             bool resc = false;
-            if (j == 0) {
+            if (i == 0) {
                 m_used = mt;
             } else if (mt > m_used + kRescaleThreshold) {
                 alpha = fast_exp2(m_used - mt);
@@ -501,8 +554,33 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             mbar_arrive(&ctl.p_full[t]);
             if (pingpong) mbar_arrive(&ctl.turn[t ^ 1]);
         }
-        // drain[t] is committed after the last PV of this tile
+        // drain[t] is committed after the last PV of this chain
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain[t], 0, abort_flag, dev_status));
+        // Split keys: chain B hands its row maximum and row sum to chain A, which merges the two
+        // partial states -- O = O_A 2^(m_A - m) + O_B 2^(m_B - m) with m = max(m_A, m_B), the
+        // sums alike -- and stores the rows.  A chain whose keys so far were all discarded has
+        // m = -inf and weight 0.
+        float w_a = 1.f, w_b = 0.f;
+        if (split) {
+            if (t == 1) {
+                ctl.split_m[r] = m_used;
+                ctl.split_l[r] = l_sum;
+                if (!ok) ctl.split_ok = 0;
+            }
+            named_barrier_sync(1, 2 * kBM);
+            if (t == 1) {
+                ok = false;                                // chain A stores the rows
+            } else if (ok) {
+                ok = ctl.split_ok &&
+                     __all_sync(0xffffffffu, wait_bar(&ctl.drain[1], 0, abort_flag, dev_status));
+                const float mb = ctl.split_m[r], lb = ctl.split_l[r];
+                const float m = fmaxf(m_used, mb);
+                w_a = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m);
+                w_b = mb == -INFINITY ? 0.f : fast_exp2(mb - m);
+                l_sum = l_sum * w_a + lb * w_b;
+                m_used = m;
+            }
+        }
         if (ok) {
             tc_fence_after();
             const int i = q0 + t * kBM + r;
@@ -513,6 +591,14 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 uint32_t o[32];
                 tmem_ld32(lane_base + col_o(t) + cc * 32, o);
                 tmem_ld_wait();
+                if (split) {
+                    uint32_t ob[32];
+                    tmem_ld32(lane_base + col_o(1) + cc * 32, ob);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        o[x] = __float_as_uint(fmaf(__uint_as_float(o[x]), w_a, __uint_as_float(ob[x]) * w_b));
+                }
                 if (orow && i < n_rows) {
                     uint32_t pkd[16];
 #pragma unroll

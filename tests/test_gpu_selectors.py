@@ -85,6 +85,31 @@ def test_dropna_slot_attention_parity(B, n_q, hq, hkv, T, dtype, d):
         assert torch.all(out[B - 1] == 0)
 
 
+@pytest.mark.parametrize("lo,hi", [(384, 700), (0, 384), (0, 700), (383, 385)])
+def test_dropna_lone_query_tile_with_a_discarded_key_half(lo, hi):
+    # One query tile and six key tiles: the kernel gives each of its two chains three key tiles
+    # and merges their partial softmax states, so discarding keys [384, 700) or [0, 384) leaves
+    # one chain with no key at all, and [0, 700) both.
+    d, hq, hkv, T, ns, n_q = 128, 2, 2, 700, 2000, 100
+    g = torch.Generator().manual_seed(lo * 7 + hi)
+    kc = torch.randn((ns, hkv, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((ns, hkv, d), generator=g).to(torch.bfloat16)
+    q = (torch.randn((1, n_q, hq, d), generator=g) * 2).to(torch.bfloat16)
+    rs = torch.randint(0, ns, (1, T), generator=g, dtype=torch.int32)
+    rs[0, lo:hi] = -1
+    ref = oracle.slot_attention(q, rs, kc, vc, scale=d ** -0.5, drop_none=True)
+    out = torch.full((1, n_q, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ac.acache_slot_attention_dropna(ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16"), 1, n_q, dev(q), T, dev(rs),
+                                    dev(kc), dev(vc), ns, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    err = np.abs(out.double().cpu().numpy() - ref)
+    assert err.max() <= 2e-2, f"max |err| {err.max():.3e}"
+    if hi - lo == T:
+        assert torch.all(out == 0)
+
+
 def test_dropna_other_negative_slots_still_flag():
     d, hq, hkv, T, ns = 128, 2, 2, 150, 300
     g = torch.Generator().manual_seed(21)
