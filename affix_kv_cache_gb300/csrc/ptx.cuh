@@ -70,6 +70,11 @@ ACACHE_DEVFN void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+ACACHE_DEVFN void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // ---- cp.async (16-byte global -> shared; src_bytes < 16 zero-fills the rest) ------------
 ACACHE_DEVFN void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -116,6 +121,21 @@ ACACHE_DEVFN void tma_gather4(uint32_t dst, const void* tmap, int col, int r0, i
         "l"(tmap), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
         : "memory");
 }
+// Tensor-map stores from shared memory (bulk-group completion).  Box rows or columns outside
+// the tensor are not written.
+ACACHE_DEVFN void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+ACACHE_DEVFN void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(tmap),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+ACACHE_DEVFN void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has read its shared-memory source.
+ACACHE_DEVFN void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 ACACHE_DEVFN void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -216,10 +236,25 @@ ACACHE_DEVFN void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" :
 // Let the next grid on the stream start its prologue before this grid has finished.
 ACACHE_DEVFN void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Named barrier `id` (1-15; 0 is the one __syncthreads uses) over `count` threads, a multiple
+// Named barrier ID with a vote: true iff `pred` holds on every one of the `count` threads.
+template <int ID>
+ACACHE_DEVFN bool named_barrier_and(uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(ID), "r"(count)
+        : "memory");
+    return r != 0;
+}
+// Named barrier ID (1-15; 0 is the one __syncthreads uses) over `count` threads, a multiple
 // of 32: whole warps of a subset of the CTA synchronise without involving the other warps.
-ACACHE_DEVFN void named_barrier_sync(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+template <int ID>
+ACACHE_DEVFN void named_barrier_sync(uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(count) : "memory");
 }
 
 // ---- thread-block clusters (distributed shared memory) ------------------------------------

@@ -92,6 +92,7 @@ struct AttnParams {
     CUtensorMap tm_v0;    // probe: 3-D affix [L][Hkv][d], box {64, 1, 128}
     CUtensorMap tm_k1;    // probe: 4-D own rows [B][P][Hkv][d], box {64, 1, 128, 1}
     CUtensorMap tm_v1;
+    CUtensorMap tm_o;     // output, laid out as tm_q (valid when out is not null)
     const int32_t* read_slot;
     const int32_t* q_start;   // ragged batches (slot keys): [B+1] query-row offsets, or null
     const int32_t* kv_start;  //                              [B+1] logical-key offsets
@@ -268,6 +269,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             // -------------------------------------------------------------- TMA producers
             if (warp == kProdWarp && lane == 0) {
                 tma_prefetch_desc(&p.tm_q);
+                if (p.out) tma_prefetch_desc(&p.tm_o);
                 tma_prefetch_desc(&p.tm_k0);
                 tma_prefetch_desc(&p.tm_v0);
                 if (kMode == kProbeKeys) {
@@ -567,7 +569,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 ctl.split_l[r] = l_sum;
                 if (!ok) ctl.split_ok = 0;
             }
-            named_barrier_sync(1, 2 * kBM);
+            named_barrier_sync<1>(2 * kBM);
             if (t == 1) {
                 ok = false;                                // chain A stores the rows
             } else if (ok) {
@@ -581,11 +583,19 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 m_used = m;
             }
         }
+        // Output rows leave through this chain's Q buffer, free once its MMAs (and with split
+        // keys chain B's) are complete, and two tensor-map stores of whole 256-byte row slices,
+        // instead of per-thread 16-byte stores scattered at the query-row stride.  A ragged
+        // batch's partial last block keeps per-thread stores: its box would reach into the next
+        // request's rows.
+        const bool writer = !split || t == 0;
+        const bool boxed = p.out && !(kMode == kSlotKeys && p.q_start && q0 + (t + 1) * kBM > n_rows);
+        const uint32_t stage = sQ(t);
         if (ok) {
             tc_fence_after();
             const int i = q0 + t * kBM + r;
             const float inv_l = (kDrop && !(l_sum > 0.f)) ? 0.f : 1.f / l_sum;
-            bf16* orow = p.out ? p.out + ((qbase + i) * p.Hq + h) * kD : nullptr;
+            bf16* orow = (p.out && !boxed) ? p.out + ((qbase + i) * p.Hq + h) * kD : nullptr;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t o[32];
@@ -599,7 +609,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     for (int x = 0; x < 32; ++x)
                         o[x] = __float_as_uint(fmaf(__uint_as_float(o[x]), w_a, __uint_as_float(ob[x]) * w_b));
                 }
-                if (orow && i < n_rows) {
+                if (boxed || (orow && i < n_rows)) {
                     uint32_t pkd[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
@@ -607,16 +617,46 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                                                                    __uint_as_float(o[2 * x + 1]) * inv_l);
                         pkd[x] = *reinterpret_cast<uint32_t*>(&two);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+                    if (boxed) {
+                        // 16-byte chunk k = 4 cc + x of row r: region k / 8, swizzled position
+                        // (k % 8) ^ (r % 8) -- the layout the 128-byte-swizzled map expects
 #pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
+                        for (int x = 0; x < 4; ++x) {
+                            const int k = 4 * cc + x;
+                            st_shared_v4(stage + (uint32_t)(k >> 3) * kRegion + (uint32_t)r * 128u +
+                                             ((uint32_t)((k & 7) ^ (r & 7)) << 4),
+                                         pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
+                        }
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
+                    }
                 }
             }
             if (p.stat_m && i < p.n_rows) {
                 const int64_t so = ((int64_t)b * p.Hq + h) * p.n_rows + i;
                 p.stat_m[so] = m_used;
                 p.stat_l[so] = l_sum;
+            }
+        }
+        if (writer && boxed) {
+            // every thread of the warpgroup arrives (ok or not); the rows go out only if all of
+            // them were written
+            fence_proxy_async_smem();
+            const bool all_ok = t == 0 ? named_barrier_and<2>(kBM, ok) : named_barrier_and<3>(kBM, ok);
+            if (r == 0 && all_ok) {
+                if (kMode == kSlotKeys && p.q_start) {
+                    const int row = (int)(qbase + q0 + t * kBM);
+                    tma_store_3d(&p.tm_o, stage, 0, h, row);
+                    tma_store_3d(&p.tm_o, stage + kRegion, 64, h, row);
+                } else {
+                    tma_store_4d(&p.tm_o, stage, 0, h, q0 + t * kBM, b);
+                    tma_store_4d(&p.tm_o, stage + kRegion, 64, h, q0 + t * kBM, b);
+                }
+                bulk_commit_group();
+                bulk_wait_group_read0();     // the buffer must outlive the reads
             }
         }
         }
@@ -880,7 +920,7 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     const uint64_t dq[4] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)n_q, (uint64_t)B};
     const uint64_t dp[2] = {(uint64_t)kD, (uint64_t)num_slots * a.hkv};
     if (!make_map(&prm.tm_q, q, 4, dq, 2, kBM) || !make_map(&prm.tm_k0, k_cache, 2, dp, 1, 1) ||
-        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1))
+        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1) || (out && !make_map(&prm.tm_o, out, 4, dq, 2, kBM)))
         return ACACHE_ERR_CUDA;
     prm.tm_k1 = prm.tm_k0;
     prm.tm_v1 = prm.tm_v0;
@@ -907,7 +947,7 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
     const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)(total_q > 0 ? total_q : 1)};
     const uint64_t dp[2] = {(uint64_t)kD, (uint64_t)num_slots * a.hkv};
     if (!make_map(&prm.tm_q, q, 3, dq, 2, kBM) || !make_map(&prm.tm_k0, k_cache, 2, dp, 1, 1) ||
-        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1))
+        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1) || (out && !make_map(&prm.tm_o, out, 3, dq, 2, kBM)))
         return ACACHE_ERR_CUDA;
     prm.tm_k1 = prm.tm_k0;
     prm.tm_v1 = prm.tm_v0;
@@ -939,7 +979,7 @@ int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, co
     const void* va = L > 0 ? v_aff : v_req;
     if (!make_map(&prm.tm_q, q, 4, dq, 2, kBM) || !make_map(&prm.tm_k0, ka, 3, da, 2, kBN) ||
         !make_map(&prm.tm_v0, va, 3, da, 2, kBN) || !make_map(&prm.tm_k1, k_req, 4, dr, 2, kBN) ||
-        !make_map(&prm.tm_v1, v_req, 4, dr, 2, kBN))
+        !make_map(&prm.tm_v1, v_req, 4, dr, 2, kBN) || (out && !make_map(&prm.tm_o, out, 4, dq, 2, kBM)))
         return ACACHE_ERR_CUDA;
     prm.out = (bf16*)out;
     prm.stat_m = stat_m;
