@@ -506,15 +506,17 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 resc = true;
             }
             if (__any_sync(0xffffffffu, resc)) {
-                // S_t(j) completed after PV_t(j-1): O_t is final up to tile j-1; rescale it
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_base + col_o(t) + cc * 32, o);
+                // S_t(j) completed after PV_t(j-1): O_t is final up to tile j-1; rescale it,
+                // 8 columns at a time (rare; the S values stay live meanwhile, so this path
+                // must not raise the loop's register peak)
+#pragma unroll 1
+                for (int q = 0; q < kD / 8; ++q) {
+                    uint32_t o[8];
+                    tmem_ld8(lane_base + col_o(t) + q * 8, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(lane_base + col_o(t) + cc * 32, o);
+                    for (int x = 0; x < 8; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+                    tmem_st8(lane_base + col_o(t) + q * 8, o);
                 }
                 tmem_st_wait();
             }

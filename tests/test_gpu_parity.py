@@ -294,6 +294,32 @@ def test_decode_slot_attention_peaked_rows():
     assert_out_close(out.float().cpu().numpy(), ref, "bf16", "peaked decode rows")
 
 
+def test_slot_attention_peaked_rows_many_queries():
+    """The 128-row tile kernel with rows whose maximum jumps late: the lazy rescale of O in TMEM
+    runs, and in the one-tile last query block (rows 256-299, keys split between two chains)
+    the two halves' maxima differ by tens of powers of two when they are merged."""
+    B, n_q, hq, hkv, T, d, num_slots = 1, 300, 2, 2, 2000, 128, 2500
+    g = torch.Generator().manual_seed(17)
+    kc = torch.randn((num_slots, hkv, d), generator=g)
+    vc = torch.randn((num_slots, hkv, d), generator=g)
+    q = torch.randn((B, n_q, hq, d), generator=g)
+    rs = torch.arange(T, dtype=torch.int32)[None].repeat(B, 1)
+    kc[1900] = q[0, 3] * 3        # two-tile block, a late key tile
+    kc[1500] = q[0, 290] * 3      # last block: in the second chain's half of the keys
+    kc[100] = q[0, 291] * 3       # last block: in the first chain's half
+    kc[130] = q[0, 200] * 2
+    kc[1990] = q[0, 200] * 3      # a second, larger jump in the same row
+    kc, vc, q = kc.to(torch.bfloat16), vc.to(torch.bfloat16), q.to(torch.bfloat16)
+    ref = oracle.slot_attention(q, rs, kc, vc, scale=d ** -0.5)
+    out = torch.empty((B, n_q, hq, d), dtype=torch.bfloat16, device="cuda")
+    st = status_tensor()
+    ac.acache_slot_attention(ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16"), B, n_q, dev(q), T, dev(rs),
+                             dev(kc), dev(vc), num_slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(out.float().cpu().numpy(), ref, "bf16", "peaked rows")
+
+
 def test_slot_attention_bad_slot_reads_zero_row():
     B, n_q, T, hq, hkv, d, num_slots = 1, 40, 150, 2, 2, 128, 300
     g = torch.Generator().manual_seed(11)
