@@ -21,10 +21,12 @@
 //             V an MN-major shared-memory operand), S_t(j+1) right after PV_t(j).  Warps 10
 //             and 11 are TMA producers.
 //   WG3       TMA producers: warps 12, 13 and 10 fill a 3-stage K ring, warps 14, 15 and 11 a
-//             2-stage V ring.  Read-slot keys: a tile is 64 `tile::gather4` loads (4 pool rows
-//             x 64 columns, rows resolved through the read-slot map one tile ahead), about 21
-//             per warp -- each gather4 a lane issues costs its warp tens of cycles, so the
-//             gather rate grows with the number of issuing warps.  Probe keys: the affix rows
+//             2-stage V ring.  Read-slot keys: a tile whose 128 slots are consecutive (a
+//             request's own rows, a page of the shared region) is two tiled box loads of the
+//             pool; any other is 64 `tile::gather4` loads (4 pool rows x 64 columns, rows
+//             resolved through the read-slot map one tile ahead), about 21 per warp -- each
+//             gather4 a lane issues costs its warp tens of cycles, so the gather rate grows
+//             with the number of issuing warps.  Probe keys: the affix rows
 //             and the request's own rows are contiguous per KV head, so a tile is two tiled
 //             box loads.  Loads complete on the stage's mbarrier by byte count.
 //   setmaxnreg gives the softmax warpgroups 200 registers and WG2 / WG3 56.
@@ -90,8 +92,8 @@ struct AttnParams {
     CUtensorMap tm_q;     // 4-D [B][n_rows][Hq][d], box {64, 1, 128, 1}
     CUtensorMap tm_k0;    // slot: 2-D pool [num_slots*Hkv][d], box {64, 1} (gather4)
     CUtensorMap tm_v0;    // probe: 3-D affix [L][Hkv][d], box {64, 1, 128}
-    CUtensorMap tm_k1;    // probe: 4-D own rows [B][P][Hkv][d], box {64, 1, 128, 1}
-    CUtensorMap tm_v1;
+    CUtensorMap tm_k1;    // slot: 3-D pool [num_slots][Hkv][d], box {64, 1, 128} (consecutive slots)
+    CUtensorMap tm_v1;    // probe: 4-D own rows [B][P][Hkv][d], box {64, 1, 128, 1}
     CUtensorMap tm_o;     // output, laid out as tm_q (valid when out is not null)
     const int32_t* read_slot;
     const int32_t* q_start;   // ragged batches (slot keys): [B+1] query-row offsets, or null
@@ -272,10 +274,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 if (p.out) tma_prefetch_desc(&p.tm_o);
                 tma_prefetch_desc(&p.tm_k0);
                 tma_prefetch_desc(&p.tm_v0);
-                if (kMode == kProbeKeys) {
-                    tma_prefetch_desc(&p.tm_k1);
-                    tma_prefetch_desc(&p.tm_v1);
-                }
+                tma_prefetch_desc(&p.tm_k1);
+                tma_prefetch_desc(&p.tm_v1);
                 mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_qt);
                 for (int t = 0; t < n_qt; ++t) {
                     if (kMode == kSlotKeys && p.q_start) {   // 3-D map over the flattened rows
@@ -307,24 +307,40 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 const int x = 3 * lane + pi;
                 const bool gathers = x < 64;
                 const int g = x >> 1, half = x & 1;
-                // rows of tile j are resolved one iteration ahead, so the read-slot loads overlap
-                // the previous tile's wait and gather issue
-                auto resolve = [&](int j, int (&rows)[4]) {
+                // Read-slot tile j, resolved one entry ahead (the loads overlap the previous tile's
+                // wait and gather issue): lane l reads the slots of keys 4l..4l+3 and the warp votes
+                // whether all 128 keys are present with consecutive slots (a request's own rows, a
+                // page of the shared region) -- then the tile is two tiled box loads of the pool
+                // (slot0 = the first slot), else 64 gather4 loads whose rows each lane takes from
+                // the lane that read them.  Every warp of the trio reads the same slots and so
+                // takes the same decision.  Invalid slots and keys past T read an out-of-range row.
+                auto resolve = [&](int j, int (&rows)[4], int& slot0) -> bool {
+                    int sl[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int t = j * kBN + 4 * g + u;
-                        rows[u] = oob_row;
-                        if (kMode == kSlotKeys && gathers && j < n_kv && t < T_len) {
-                            const int64_t slot = p.read_slot[kbase + t];
+                        const int tk = j * kBN + 4 * lane + u;
+                        sl[u] = -1;
+                        if (kMode == kSlotKeys && j < n_kv && tk < T_len) {
+                            const int slot = p.read_slot[kbase + tk];
                             if (slot >= 0 && slot < p.num_slots)
-                                rows[u] = (int)(slot * p.Hkv + hk);
-                            else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
+                                sl[u] = slot;
+                            else if (!is_v && pi == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
                                 flag(dev_status, ACACHE_DEV_BAD_SLOT);
                         }
                     }
+                    bool run = sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 && sl[3] == sl[0] + 3;
+                    const int after = __shfl_down_sync(0xffffffffu, sl[0], 1);
+                    if (lane < 31) run = run && after == sl[0] + 4;
+                    slot0 = __shfl_sync(0xffffffffu, sl[0], 0);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int sv = __shfl_sync(0xffffffffu, sl[u], g & 31);
+                        rows[u] = (gathers && sv >= 0) ? sv * p.Hkv + hk : oob_row;
+                    }
+                    return __all_sync(0xffffffffu, run);
                 };
-                int next[4];
-                resolve(ks.entry_tile(0), next);
+                int next[4], next_slot0;
+                bool next_box = resolve(ks.entry_tile(0), next, next_slot0);
                 // store-then-attend: the pool rows this launch reads may have been written by the
                 // preceding store grid (launched ahead with programmatic stream serialisation)
                 grid_dependency_wait();
@@ -333,7 +349,9 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     const int j = ks.entry_tile(e);           // the key tile entry e holds
                     const uint32_t dst_tile = is_v ? sVs(s) : sK(s);
                     int rows[4] = {next[0], next[1], next[2], next[3]};
-                    resolve(e + 1 < n_kv ? ks.entry_tile(e + 1) : n_kv, next);
+                    const int slot0 = next_slot0;
+                    const bool box = next_box;
+                    next_box = resolve(e + 1 < n_kv ? ks.entry_tile(e + 1) : n_kv, next, next_slot0);
                     if (e >= nst &&
                         !__all_sync(0xffffffffu, wait_bar(&empty[s], ((e / nst) - 1) & 1, abort_flag,
                                                           dev_status)))
@@ -343,9 +361,15 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
                     __syncwarp();
                     if (kMode == kSlotKeys) {
-                        if (gathers)
+                        if (box) {
+                            if (leader) {
+                                tma_load_3d(dst_tile, tm_own, 0, hk, slot0, &full[s]);
+                                tma_load_3d(dst_tile + kRegion, tm_own, 64, hk, slot0, &full[s]);
+                            }
+                        } else if (gathers) {
                             tma_gather4(dst_tile + (uint32_t)half * kRegion + (uint32_t)g * 512u, tm_aff, half * 64,
                                         rows[0], rows[1], rows[2], rows[3], &full[s]);
+                        }
                     } else if (lane == 0) {
                         if (j < n_aff) {
                             const int j0 = j * kBN;
@@ -921,11 +945,11 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     AttnParams prm{};
     const uint64_t dq[4] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)n_q, (uint64_t)B};
     const uint64_t dp[2] = {(uint64_t)kD, (uint64_t)num_slots * a.hkv};
+    const uint64_t d3[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)num_slots};
     if (!make_map(&prm.tm_q, q, 4, dq, 2, kBM) || !make_map(&prm.tm_k0, k_cache, 2, dp, 1, 1) ||
-        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1) || (out && !make_map(&prm.tm_o, out, 4, dq, 2, kBM)))
+        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1) || !make_map(&prm.tm_k1, k_cache, 3, d3, 2, kBN) ||
+        !make_map(&prm.tm_v1, v_cache, 3, d3, 2, kBN) || (out && !make_map(&prm.tm_o, out, 4, dq, 2, kBM)))
         return ACACHE_ERR_CUDA;
-    prm.tm_k1 = prm.tm_k0;
-    prm.tm_v1 = prm.tm_v0;
     prm.read_slot = read_slot;
     prm.out = (bf16*)out;
     prm.dev_status = dev_status;
@@ -948,11 +972,11 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
     AttnParams prm{};
     const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)(total_q > 0 ? total_q : 1)};
     const uint64_t dp[2] = {(uint64_t)kD, (uint64_t)num_slots * a.hkv};
+    const uint64_t d3[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)num_slots};
     if (!make_map(&prm.tm_q, q, 3, dq, 2, kBM) || !make_map(&prm.tm_k0, k_cache, 2, dp, 1, 1) ||
-        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1) || (out && !make_map(&prm.tm_o, out, 3, dq, 2, kBM)))
+        !make_map(&prm.tm_v0, v_cache, 2, dp, 1, 1) || !make_map(&prm.tm_k1, k_cache, 3, d3, 2, kBN) ||
+        !make_map(&prm.tm_v1, v_cache, 3, d3, 2, kBN) || (out && !make_map(&prm.tm_o, out, 3, dq, 2, kBM)))
         return ACACHE_ERR_CUDA;
-    prm.tm_k1 = prm.tm_k0;
-    prm.tm_v1 = prm.tm_v0;
     prm.read_slot = read_slot;
     prm.q_start = q_start;
     prm.kv_start = kv_start;

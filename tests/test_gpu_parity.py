@@ -320,6 +320,38 @@ def test_slot_attention_peaked_rows_many_queries():
     assert_out_close(out.float().cpu().numpy(), ref, "bf16", "peaked rows")
 
 
+@pytest.mark.parametrize("drop", [False, True])
+def test_slot_attention_consecutive_slot_tiles(drop):
+    """Read-slot tiles whose 128 slots are consecutive load as tiled boxes, others gather: tiles
+    consecutive from slot 100, from slot 0, and ending on the pool's last slot; one with a single
+    key out of order; a random one; a ragged last tile that is consecutive; with DropNA, a
+    consecutive tile with one discarded key."""
+    B, n_q, hq, hkv, T, d, num_slots = 2, 300, 2, 2, 700, 128, 1200
+    g = torch.Generator().manual_seed(23 + drop)
+    kc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    q = torch.randn((B, n_q, hq, d), generator=g).to(torch.bfloat16)
+    rs = torch.randint(0, num_slots, (B, T), generator=g, dtype=torch.int32)
+    ar = torch.arange(128, dtype=torch.int32)
+    rs[:, 0:128] = 100 + ar                          # consecutive
+    rs[:, 128:256] = 400 + ar
+    rs[:, 200], rs[:, 201] = rs[:, 201].clone(), rs[:, 200].clone()   # one pair swapped: gathers
+    rs[:, 256:384] = num_slots - 128 + ar            # ends on the last slot
+    rs[1, 512:640] = ar                              # request 1: consecutive from 0
+    rs[:, 640:700] = 700 + ar[:60]                   # ragged last tile, consecutive
+    if drop:
+        rs[0, 300] = -1                              # a discarded key inside a consecutive tile
+    ref = oracle.slot_attention(q, rs, kc, vc, scale=d ** -0.5, drop_none=drop)
+    out = torch.empty((B, n_q, hq, d), dtype=torch.bfloat16, device="cuda")
+    st = status_tensor()
+    desc = ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16")
+    fn = ac.acache_slot_attention_dropna if drop else ac.acache_slot_attention
+    fn(desc, B, n_q, dev(q), T, dev(rs), dev(kc), dev(vc), num_slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(out.float().cpu().numpy(), ref, "bf16", "consecutive-slot tiles")
+
+
 def test_slot_attention_bad_slot_reads_zero_row():
     B, n_q, T, hq, hkv, d, num_slots = 1, 40, 150, 2, 2, 128, 300
     g = torch.Generator().manual_seed(11)
