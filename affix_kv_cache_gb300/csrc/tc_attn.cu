@@ -181,6 +181,25 @@ ACACHE_DEVFN int tile_valid(const AttnParams& p, int j, int T_len) {
     return j < n_aff ? min(kBN, p.L - j * kBN) : min(kBN, p.P - (j - n_aff) * kBN);
 }
 
+// Read-slot entries of keys 4 lane .. 4 lane + 3 of key tile j: -1 where there is no key or
+// the slot lies outside the pool (flagged by `flagger` unless it marks a discarded key).
+template <bool kDrop>
+ACACHE_DEVFN void tile_slots(const AttnParams& p, int64_t kbase, int T_len, int n_kv, int j, int lane,
+                             bool flagger, int (&sl)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int tk = j * kBN + 4 * lane + u;
+        sl[u] = -1;
+        if (j < n_kv && tk < T_len) {
+            const int slot = p.read_slot[kbase + tk];
+            if (slot >= 0 && slot < p.num_slots)
+                sl[u] = slot;
+            else if (flagger && !(kDrop && slot == ACACHE_SLOT_NONE))
+                flag(p.dev_status, ACACHE_DEV_BAD_SLOT);
+        }
+    }
+}
+
 // kDrop (read-slot keys only): a read-slot entry equal to ACACHE_SLOT_NONE marks a logical
 // position whose K/V was discarded (the page's DropNA ablation, Sec. 5.3): the key takes
 // no part in the softmax, and a row with no key left outputs zeros.
@@ -231,6 +250,14 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
+    // The first key tile's read-slot entries are read by the producer lanes before the set-up
+    // below, which hides their latency (warp 12 flags bad slots; see the producers).  The maps
+    // are not written by a store grid this launch may overlap.
+    const bool prod_warp = warp >= kMmaWarp + 2;
+    const bool flagger = warp == kProdWarp;
+    int sl0[4] = {-1, -1, -1, -1};
+    if (kMode == kSlotKeys && prod_warp)
+        tile_slots<kDrop>(p, kbase, T_len, n_kv, ks.entry_tile(0), lane, flagger, sl0);
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 1);
@@ -255,6 +282,18 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         ctl.abort = 0;
         ctl.split_ok = 1;
         fence_mbar_init();
+        // the Q tiles, as soon as their barrier exists
+        mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_qt);
+        for (int t = 0; t < n_qt; ++t) {
+            if (kMode == kSlotKeys && p.q_start) {   // 3-D map over the flattened rows
+                const int r = (int)(qbase + q0 + t * kBM);
+                tma_load_3d(sQ(t), &p.tm_q, 0, h, r, &ctl.q_full);
+                tma_load_3d(sQ(t) + kRegion, &p.tm_q, 64, h, r, &ctl.q_full);
+            } else {
+                tma_load_4d(sQ(t), &p.tm_q, 0, h, q0 + t * kBM, b, &ctl.q_full);
+                tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, h, q0 + t * kBM, b, &ctl.q_full);
+            }
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&ctl.tmem_base, kTmemCols);
@@ -272,23 +311,11 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
         if (warp >= kMmaWarp + 2) {
             // -------------------------------------------------------------- TMA producers
             if (warp == kProdWarp && lane == 0) {
-                tma_prefetch_desc(&p.tm_q);
                 if (p.out) tma_prefetch_desc(&p.tm_o);
                 tma_prefetch_desc(&p.tm_k0);
                 tma_prefetch_desc(&p.tm_v0);
                 tma_prefetch_desc(&p.tm_k1);
                 tma_prefetch_desc(&p.tm_v1);
-                mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_qt);
-                for (int t = 0; t < n_qt; ++t) {
-                    if (kMode == kSlotKeys && p.q_start) {   // 3-D map over the flattened rows
-                        const int r = (int)(qbase + q0 + t * kBM);
-                        tma_load_3d(sQ(t), &p.tm_q, 0, h, r, &ctl.q_full);
-                        tma_load_3d(sQ(t) + kRegion, &p.tm_q, 64, h, r, &ctl.q_full);
-                    } else {
-                        tma_load_4d(sQ(t), &p.tm_q, 0, h, q0 + t * kBM, b, &ctl.q_full);
-                        tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, h, q0 + t * kBM, b, &ctl.q_full);
-                    }
-                }
             }
             // warps 12, 13 and 10 fill the K ring, warps 14, 15 and 11 the V ring (a gather4 costs
             // its warp tens of cycles of issue, so the tile's 64 are spread over three warps); probe
@@ -316,20 +343,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 // (slot0 = the first slot), else 64 gather4 loads whose rows each lane takes from
                 // the lane that read them.  Every warp of the trio reads the same slots and so
                 // takes the same decision.  Invalid slots and keys past T read an out-of-range row.
-                auto resolve = [&](int j, int (&rows)[4], int& slot0) -> bool {
-                    int sl[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int tk = j * kBN + 4 * lane + u;
-                        sl[u] = -1;
-                        if (kMode == kSlotKeys && j < n_kv && tk < T_len) {
-                            const int slot = p.read_slot[kbase + tk];
-                            if (slot >= 0 && slot < p.num_slots)
-                                sl[u] = slot;
-                            else if (!is_v && pi == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
-                                flag(dev_status, ACACHE_DEV_BAD_SLOT);
-                        }
-                    }
+                auto finish = [&](const int (&sl)[4], int (&rows)[4], int& slot0) -> bool {
                     bool run = sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 && sl[3] == sl[0] + 3;
                     const int after = __shfl_down_sync(0xffffffffu, sl[0], 1);
                     if (lane < 31) run = run && after == sl[0] + 4;
@@ -341,8 +355,13 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     }
                     return __all_sync(0xffffffffu, run);
                 };
+                auto resolve = [&](int j, int (&rows)[4], int& slot0) -> bool {
+                    int sl[4];
+                    if (kMode == kSlotKeys) tile_slots<kDrop>(p, kbase, T_len, n_kv, j, lane, flagger, sl);
+                    return finish(sl, rows, slot0);
+                };
                 int next[4], next_slot0;
-                bool next_box = resolve(ks.entry_tile(0), next, next_slot0);
+                bool next_box = finish(sl0, next, next_slot0);
                 // store-then-attend: the pool rows this launch reads may have been written by the
                 // preceding store grid (launched ahead with programmatic stream serialisation)
                 grid_dependency_wait();
