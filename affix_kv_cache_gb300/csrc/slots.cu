@@ -4,10 +4,9 @@
 // recomputation map, per-request read-slot map), Sec. 4.2 (maps recorded at admission),
 // Sec. 4.3 and App. C.1 (store-then-attend).
 //
-// The copies are HBM-bound: every thread moves 16-byte vectors, keeps kUnroll
-// independent loads in flight before its stores, and the grid is a multiple of the SM
-// count.  Slot indices are read once per 16-byte chunk (they hit L1: all chunks of a
-// row share one index).
+// The copies are HBM-bound: every thread moves 16-byte vectors and keeps kUnroll
+// independent loads in flight before its stores; a warp copies one row, reading its slot
+// index once; the grid is capped at 8 CTAs per SM.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -17,51 +16,51 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kUnroll = 4;
 
-// Row copy through an index table.  Rows are `cpr` 16-byte chunks long.
+// Row copy through an index table, one warp per part of a row of K or of V (2 * nrows rows,
+// `parts` parts of `per_part` 16-byte chunks each -- several warps per row when rows are few):
+// the row's index is read once and the lanes stride over the part's chunks, kUnroll loads in
+// flight each, with no per-chunk index arithmetic.
 //   scatter = true : dst[idx[r]] = src[r]   (store step, idx = write slots)
 //   scatter = false: dst[r] = src[idx[r]]   (gather through the read-slot map)
 template <bool kScatter>
 __global__ void __launch_bounds__(kCopyThreads)
 indexed_row_copy(const int32_t* __restrict__ idx, int64_t nrows, int64_t cpr,
+                 int parts, int64_t per_part,
                  const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
                  uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
                  int64_t num_slots, int64_t private_begin, int32_t* dev_status) {
     // a grid that waits on this copy (store-then-attend) may start its prologue now; it
     // reads nothing this copy writes before its own grid-dependency wait
     ptx::grid_launch_dependents();
-    const int64_t total = nrows * cpr;                   // chunks per tensor (K or V)
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < 2 * total;
-         base += stride * kUnroll) {
-        uint4 val[kUnroll];
-        uint4* dst[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t c = base + u * stride;
-            dst[u] = nullptr;
-            if (c < 2 * total) {
-                const bool is_v = c >= total;
-                const int64_t cc = is_v ? c - total : c;
-                const int64_t r = cc / cpr, w = cc - r * cpr;
-                const int64_t slot = idx[r];
-                bool good = slot >= 0 && slot < num_slots;
-                if (!good) {
-                    if (w == 0 && !is_v) flag(dev_status, ACACHE_DEV_BAD_SLOT);
-                } else if (kScatter && slot < private_begin) {
-                    good = false;
-                    if (w == 0 && !is_v) flag(dev_status, ACACHE_DEV_SHARED_WRITE);
-                }
-                if (good) {
-                    const int64_t s_off = kScatter ? r * cpr + w : slot * cpr + w;
-                    const int64_t d_off = kScatter ? slot * cpr + w : r * cpr + w;
-                    val[u] = __ldcs((is_v ? src_v : src_k) + s_off);   // streamed once
-                    dst[u] = (is_v ? dst_v : dst_k) + d_off;
-                }
-            }
+    constexpr int kWarps = kCopyThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t n_warps = (int64_t)gridDim.x * kWarps;
+    for (int64_t w = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); w < 2 * nrows * parts; w += n_warps) {
+        const int64_t wr = w / parts;                    // row of K (< nrows) or of V
+        const int part = (int)(w - wr * parts);
+        const bool is_v = wr >= nrows;
+        const int64_t r = is_v ? wr - nrows : wr;
+        const int64_t slot = idx[r];
+        if (slot < 0 || slot >= num_slots) {
+            if (!is_v && part == 0 && lane == 0) flag(dev_status, ACACHE_DEV_BAD_SLOT);
+            continue;
         }
+        if (kScatter && slot < private_begin) {
+            if (!is_v && part == 0 && lane == 0) flag(dev_status, ACACHE_DEV_SHARED_WRITE);
+            continue;
+        }
+        const int64_t c_end = (part + 1) * per_part < cpr ? (part + 1) * per_part : cpr;
+        const uint4* src = (is_v ? src_v : src_k) + (kScatter ? r : slot) * cpr;
+        uint4* dst = (is_v ? dst_v : dst_k) + (kScatter ? slot : r) * cpr;
+        for (int64_t c0 = part * per_part + lane; c0 < c_end; c0 += 32 * kUnroll) {
+            uint4 val[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (dst[u]) __stcs(dst[u], val[u]);
+            for (int u = 0; u < kUnroll; ++u)
+                if (c0 + 32 * u < c_end) val[u] = __ldcs(src + c0 + 32 * u);   // streamed once
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                if (c0 + 32 * u < c_end) __stcs(dst + c0 + 32 * u, val[u]);
+        }
     }
 }
 
@@ -114,9 +113,26 @@ build_maps_kernel(int T, int l, int L, int K, const int32_t* __restrict__ anchor
     }
 }
 
-int copy_grid(int64_t chunks) {
-    const int64_t per_cta = (int64_t)kCopyThreads * kUnroll;
-    int64_t want = (chunks + per_cta - 1) / per_cta;
+// Parts per row: enough warps to cover the SMs' memory latency (16 per SM) when rows are few,
+// but at least 32 * kUnroll chunks per part.
+struct CopyShape {
+    int parts;
+    int64_t per_part;
+};
+CopyShape copy_shape(int64_t rows, int64_t cpr) {      // rows: of K and V together
+    const int64_t want_warps = (int64_t)sm_count() * 16;
+    int64_t parts = (want_warps + rows - 1) / rows;
+    const int64_t max_parts = cpr / (32 * kUnroll) > 1 ? cpr / (32 * kUnroll) : 1;
+    if (parts > max_parts) parts = max_parts;
+    if (parts < 1) parts = 1;
+    int64_t per_part = (cpr + parts - 1) / parts;
+    per_part = (per_part + 31) / 32 * 32;
+    return {(int)parts, per_part};
+}
+
+int copy_grid(int64_t items) {                      // one warp per part of a row of K or V
+    const int64_t per_cta = kCopyThreads / 32;
+    int64_t want = (items + per_cta - 1) / per_cta;
     const int64_t cap = (int64_t)sm_count() * 8;     // 8 resident CTAs of 256 threads per SM
     if (want > cap) want = cap;
     if (want < 1) want = 1;
@@ -131,8 +147,9 @@ int launch_write_slots(int batch, int rows, const int32_t* write_slot, const voi
                        cudaStream_t stream) {
     const int64_t nrows = (int64_t)batch * rows, cpr = row_bytes / 16;
     if (nrows == 0) return ACACHE_OK;
-    indexed_row_copy<true><<<copy_grid(2 * nrows * cpr), kCopyThreads, 0, stream>>>(
-        write_slot, nrows, cpr, (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache,
+    const CopyShape cs = copy_shape(2 * nrows, cpr);
+    indexed_row_copy<true><<<copy_grid(2 * nrows * cs.parts), kCopyThreads, 0, stream>>>(
+        write_slot, nrows, cpr, cs.parts, cs.per_part, (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache,
         (uint4*)v_cache, num_slots, private_begin, dev_status);
     return launch_status();
 }
@@ -142,8 +159,9 @@ int launch_gather_slots(int batch, int seq_len, const int32_t* read_slot, const 
                         void* v_out, int32_t* dev_status, cudaStream_t stream) {
     const int64_t nrows = (int64_t)batch * seq_len, cpr = row_bytes / 16;
     if (nrows == 0) return ACACHE_OK;
-    indexed_row_copy<false><<<copy_grid(2 * nrows * cpr), kCopyThreads, 0, stream>>>(
-        read_slot, nrows, cpr, (const uint4*)k_cache, (const uint4*)v_cache, (uint4*)k_out,
+    const CopyShape cs = copy_shape(2 * nrows, cpr);
+    indexed_row_copy<false><<<copy_grid(2 * nrows * cs.parts), kCopyThreads, 0, stream>>>(
+        read_slot, nrows, cpr, cs.parts, cs.per_part, (const uint4*)k_cache, (const uint4*)v_cache, (uint4*)k_out,
         (uint4*)v_out, num_slots, 0, dev_status);
     return launch_status();
 }
