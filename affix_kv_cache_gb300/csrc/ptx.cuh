@@ -47,20 +47,6 @@ ACACHE_DEVFN bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// As mbar_try_wait, but the thread may be suspended for up to `ns` nanoseconds while the phase
-// is incomplete (it resumes as soon as the phase completes), instead of polling.
-ACACHE_DEVFN bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase with the given parity to complete; false after `budget` cycles.
 ACACHE_DEVFN bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget) {
     if (mbar_try_wait(bar, parity)) return true;

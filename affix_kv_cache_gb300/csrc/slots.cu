@@ -14,7 +14,7 @@ namespace acache {
 namespace {
 
 constexpr int kCopyThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 
 // Row copy through an index table, one warp per part of a row of K or of V (2 * nrows rows,
 // `parts` parts of `per_part` 16-byte chunks each -- several warps per row when rows are few):

@@ -148,15 +148,13 @@ struct KeySchedule {
     }
 };
 
-// Bounded wait that also leaves early once another role has aborted.  While the phase is
-// incomplete the thread sleeps in the barrier (woken by its completion) rather than polling,
-// which leaves the issue slots to the warps that compute.
+// Bounded wait that also leaves early once another role has aborted.
 ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                            int32_t* dev_status) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kBudget) {
             *abort_flag = 1;

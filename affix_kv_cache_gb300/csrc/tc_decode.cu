@@ -98,7 +98,7 @@ ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_f
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;   // sleeps until completion
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kBudget) {
             *abort_flag = 1;

@@ -406,6 +406,45 @@ def store_attend_compare(path, reps=3):
     return res
 
 
+def copy_bandwidth(path, peaks, reps=3):
+    """The two HBM-bound copies alone, over every layer: the store (anchor_write of the R fresh
+    rows per request) and the logical-KV gather through the read-slot map (acache_gather_slots,
+    T rows per request).  Algorithmic bytes per launch = every row read once + written once,
+    K and V; GB/s from CUDA events around `reps` passes."""
+    ac, w, lay = path.ac, path.w, path.lay
+    row = w.hkv * w.d * torch.tensor([], dtype=w.torch_dtype).element_size()
+    k_out = torch.empty((w.batch, w.T, w.hkv, w.d), dtype=w.torch_dtype, device="cuda")
+    v_out = torch.empty_like(k_out)
+
+    def store():
+        for n in range(w.layers):
+            r = path.rec[n]
+            ac.acache_write_slots(path.desc, w.batch, w.R, lay.private_slots, r["k_new"], r["v_new"],
+                                  path.kc[n], path.vc[n], lay.num_slots, lay.private_begin)
+
+    def gather():
+        for n in range(w.layers):
+            ac.acache_gather_slots(path.desc, w.batch, w.T, path.read_slot, path.kc[n], path.vc[n],
+                                   lay.num_slots, k_out, v_out)
+
+    res = {}
+    for name, fn, rows in (("store", store, w.batch * w.R), ("gather", gather, w.batch * w.T)):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / (reps * w.layers)
+        nbytes = 2 * 2 * rows * row                      # K and V, read once and written once
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"ms_per_launch": ms, "bytes_per_launch": nbytes, "gbs": gbs,
+                     "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} HBM copy"}
+    return res
+
+
 # ----------------------------------------------------------------------------- oracle
 def cpu_oracle_sample(w, budget_s):
     """Time the oracle as it stands on a bounded sample of the workload: request 0, layer by
@@ -653,6 +692,7 @@ def main():
     if not args.no_decode:
         decode = Decode(path).measure(max(args.steps, 5), 3, peaks)
     fused = store_attend_compare(path)
+    copies = copy_bandwidth(path, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -681,6 +721,7 @@ def main():
             "decode": decode,
             "store_then_attend": {"timing": "CUDA events, one recompute point over all layers, 3 passes",
                                   **fused},
+            "copies": {"timing": "CUDA events, every layer, 3 passes", **copies},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": path.launches_per_step * args.steps,
