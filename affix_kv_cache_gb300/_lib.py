@@ -32,7 +32,8 @@ EXPORTS = ("acache_status_string", "acache_version", "acache_probe_workspace_byt
            "acache_probe_scores", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
            "acache_write_slots", "acache_slot_attention", "acache_gather_slots",
            "acache_kv_deviation_scores", "acache_slot_attention_dropna", "acache_slot_attention_varlen",
-           "acache_store_attend", "acache_rerotate_keys", "acache_pool_create", "acache_pool_destroy",
+           "acache_store_attend", "acache_store_attend_layers", "acache_rerotate_keys", "acache_pool_create",
+           "acache_pool_destroy",
            "acache_pool_register_affix", "acache_pool_release_affix", "acache_pool_alloc_private",
            "acache_pool_free_private", "acache_pool_stats")
 
@@ -85,6 +86,7 @@ def lib() -> ctypes.CDLL:
             "acache_slot_attention_dropna": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
             "acache_slot_attention_varlen": (I, [D, I, P, I, I, P, P, I, P, P, P, I64, P, I, P, P]),
             "acache_store_attend": (I, [D, I, I, P, P, P, P, P, I64, I64, I, P, I, P, P, P, P]),
+            "acache_store_attend_layers": (I, [D, I, I, I, P, P, P, P, P, I64, I64, I, P, I, P, P, P, P]),
             "acache_rerotate_keys": (I, [D, I64, P, P, ctypes.c_int32, ctypes.c_double, I, P]),
             "acache_pool_create": (I, [I64, I64, ctypes.c_int32, ctypes.POINTER(P)]),
             "acache_pool_destroy": (None, [P]),
@@ -230,6 +232,31 @@ def acache_slot_attention_varlen(desc, batch, q_start, max_q_rows, total_q_rows,
                                             _p(read_slot), _p(k_cache), _p(v_cache), num_slots, _p(out),
                                             int(bool(drop_none)), _p(dev_status), _stream(stream))
     return _check("acache_slot_attention_varlen", st) if check else st
+
+
+def _ptr_array(ts, n):
+    """Host array of n device pointers (None when ts is None)."""
+    if ts is None:
+        return None
+    if len(ts) != n:
+        raise ValueError(f"expected {n} per-layer tensors, got {len(ts)}")
+    arr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def acache_store_attend_layers(desc, batch, rows, write_slot, k_new, v_new, k_cache, v_cache, num_slots,
+                               private_begin, n_q, q, seq_len, read_slot, out, dev_status=None, stream=None,
+                               check=True):
+    """Store-then-attend for every layer of a recompute point in one call (see include/acache.h);
+    the per-layer arguments are lists of tensors, one per layer."""
+    layers = len(k_cache)
+    keep = [_ptr_array(x, layers) for x in (k_new, v_new, k_cache, v_cache, q, out)]
+    ptrs = [k[0] if k is not None else None for k in keep]
+    st = lib().acache_store_attend_layers(ctypes.byref(desc), layers, batch, rows, _p(write_slot), ptrs[0],
+                                          ptrs[1], ptrs[2], ptrs[3], num_slots, private_begin, n_q, ptrs[4],
+                                          seq_len, _p(read_slot), ptrs[5], _p(dev_status), _stream(stream))
+    del keep
+    return _check("acache_store_attend_layers", st) if check else st
 
 
 def acache_store_attend(desc, batch, rows, write_slot, k_new, v_new, k_cache, v_cache, num_slots,

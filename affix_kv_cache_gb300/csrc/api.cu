@@ -266,6 +266,89 @@ int acache_store_attend(const acache_attn_desc* desc, int batch, int rows, const
                           dev_status, stream, false, store && tc_supported(a));
 }
 
+int acache_store_attend_layers(const acache_attn_desc* desc, int layers, int batch, int rows,
+                               const int32_t* write_slot, const void* const* k_new, const void* const* v_new,
+                               void* const* k_cache, void* const* v_cache, int64_t num_slots,
+                               int64_t private_begin, int n_q, const void* const* q, int seq_len,
+                               const int32_t* read_slot, void* const* out, int32_t* dev_status,
+                               void* stream) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (layers < 0 || batch < 0 || rows < 0 || n_q < 0 || seq_len < 0 || num_slots < 0 ||
+        private_begin < 0 || private_begin > num_slots)
+        return ACACHE_ERR_INVALID_ARG;
+    if (layers == 0 || batch == 0) return ACACHE_OK;
+    const bool store = rows > 0, attend = n_q > 0;
+    if (!k_cache || !v_cache || (store && (!k_new || !v_new || !write_slot)) ||
+        (attend && (!q || !out || !read_slot || seq_len == 0)))
+        return ACACHE_ERR_INVALID_ARG;
+    // every layer's arguments are checked before anything is launched
+    for (int l = 0; l < layers; ++l) {
+        if (!k_cache[l] || !v_cache[l] || !aligned16(k_cache[l]) || !aligned16(v_cache[l]))
+            return ACACHE_ERR_INVALID_ARG;
+        if (store && (!k_new[l] || !v_new[l] || !aligned16(k_new[l]) || !aligned16(v_new[l])))
+            return ACACHE_ERR_INVALID_ARG;
+        if (attend && (!q[l] || !out[l] || !aligned16(q[l]) || !aligned16(out[l])))
+            return ACACHE_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t eb = elem_bytes(a.dtype);
+    const int64_t row_bytes = (int64_t)a.hkv * a.d * eb;
+    // Byte ranges of each layer's buffers; a layer's written ranges (its pools, its output) must
+    // meet no range of another layer for their grids to overlap.
+    struct Range {
+        uintptr_t lo, hi;
+        bool written;
+    };
+    auto span = [](const void* ptr, int64_t bytes, bool written) {
+        return Range{(uintptr_t)ptr, (uintptr_t)ptr + (uintptr_t)bytes, written};
+    };
+    const int64_t pool_bytes = num_slots * row_bytes;
+    const int64_t new_bytes = (int64_t)batch * rows * row_bytes;
+    const int64_t qo_bytes = (int64_t)batch * n_q * a.hq * a.d * eb;
+    bool disjoint = true;
+    for (int i = 0; i < layers && disjoint; ++i) {
+        Range wi[3] = {span(k_cache[i], pool_bytes, true), span(v_cache[i], pool_bytes, true),
+                       span(attend ? out[i] : nullptr, attend ? qo_bytes : 0, true)};
+        for (int j = 0; j < layers && disjoint; ++j) {
+            if (i == j) continue;
+            Range rj[6] = {span(k_cache[j], pool_bytes, true), span(v_cache[j], pool_bytes, true),
+                           span(attend ? out[j] : nullptr, attend ? qo_bytes : 0, true),
+                           span(attend ? q[j] : nullptr, attend ? qo_bytes : 0, false),
+                           span(store ? k_new[j] : nullptr, store ? new_bytes : 0, false),
+                           span(store ? v_new[j] : nullptr, store ? new_bytes : 0, false)};
+            for (const Range& x : wi)
+                for (const Range& y : rj)
+                    if (x.lo < x.hi && y.lo < y.hi && x.lo < y.hi && y.lo < x.hi) disjoint = false;
+        }
+    }
+    const bool chain = disjoint && layers > 1 && (!attend || (tc_supported(a) && !tc_decode_preferred(a, n_q)));
+    if (!chain) {
+        for (int l = 0; l < layers; ++l)
+            if (int rc = acache_store_attend(desc, batch, rows, write_slot, store ? k_new[l] : nullptr,
+                                             store ? v_new[l] : nullptr, k_cache[l], v_cache[l], num_slots,
+                                             private_begin, n_q, attend ? q[l] : nullptr, seq_len, read_slot,
+                                             attend ? out[l] : nullptr, dev_status, stream))
+                return rc;
+        return ACACHE_OK;
+    }
+    // Chained: the stores of every layer back to back, then the attentions; each grid may start
+    // on the SMs its predecessor's last wave leaves idle.  The first attention is an ordinary
+    // launch, so it starts after every store of the call (and every earlier grid) is complete;
+    // the attentions chained after it start only once all of its CTAs are running.
+    if (store)
+        for (int l = 0; l < layers; ++l)
+            if (int rc = launch_write_slots(batch, rows, write_slot, k_new[l], v_new[l], k_cache[l], v_cache[l],
+                                            row_bytes, num_slots, private_begin, dev_status, st, l > 0))
+                return rc;
+    if (attend)
+        for (int l = 0; l < layers; ++l)
+            if (int rc = launch_tc_slot_attention(a, batch, n_q, q[l], seq_len, read_slot, k_cache[l], v_cache[l],
+                                                  num_slots, out[l], dev_status, st, false, false, l > 0))
+                return rc;
+    return ACACHE_OK;
+}
+
 int acache_write_slots(const acache_attn_desc* desc, int batch, int rows,
                        const int32_t* write_slot, const void* k_new, const void* v_new,
                        void* k_cache, void* v_cache, int64_t num_slots, int64_t private_begin,

@@ -119,7 +119,7 @@ int launch_score_reduce(int B, int Hq, int L, const float* partial, float* score
 int launch_write_slots(int batch, int rows, const int32_t* write_slot, const void* k_new,
                        const void* v_new, void* k_cache, void* v_cache, int64_t row_bytes,
                        int64_t num_slots, int64_t private_begin, int32_t* dev_status,
-                       cudaStream_t stream);
+                       cudaStream_t stream, bool pdl = false);
 int launch_gather_slots(int batch, int seq_len, const int32_t* read_slot, const void* k_cache,
                         const void* v_cache, int64_t row_bytes, int64_t num_slots, void* k_out,
                         void* v_out, int32_t* dev_status, cudaStream_t stream);

@@ -141,16 +141,37 @@ int copy_grid(int64_t items) {                      // one warp per part of a ro
 
 }  // namespace
 
+// pdl: launched with programmatic stream serialisation after a grid that touches none of this
+// store's memory (the store of another layer): it may run alongside that grid.
 int launch_write_slots(int batch, int rows, const int32_t* write_slot, const void* k_new,
                        const void* v_new, void* k_cache, void* v_cache, int64_t row_bytes,
                        int64_t num_slots, int64_t private_begin, int32_t* dev_status,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, bool pdl) {
     const int64_t nrows = (int64_t)batch * rows, cpr = row_bytes / 16;
     if (nrows == 0) return ACACHE_OK;
     const CopyShape cs = copy_shape(2 * nrows, cpr);
-    indexed_row_copy<true><<<copy_grid(2 * nrows * cs.parts), kCopyThreads, 0, stream>>>(
-        write_slot, nrows, cpr, cs.parts, cs.per_part, (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache,
-        (uint4*)v_cache, num_slots, private_begin, dev_status);
+    const unsigned grid = (unsigned)copy_grid(2 * nrows * cs.parts);
+    if (!pdl) {
+        indexed_row_copy<true><<<grid, kCopyThreads, 0, stream>>>(
+            write_slot, nrows, cpr, cs.parts, cs.per_part, (const uint4*)k_new, (const uint4*)v_new,
+            (uint4*)k_cache, (uint4*)v_cache, num_slots, private_begin, dev_status);
+        return launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCopyThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, indexed_row_copy<true>, write_slot, nrows, cpr, cs.parts, cs.per_part,
+                           (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache, (uint4*)v_cache,
+                           num_slots, private_begin, dev_status) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ACACHE_ERR_CUDA;
+    }
     return launch_status();
 }
 

@@ -103,6 +103,7 @@ struct AttnParams {
     float* stat_l;
     int32_t* dev_status;
     int64_t num_slots;
+    int early_wait;       // 1: the pool may have been written by the grid this one follows
     int n_rows, Hq, Hkv, T_len, L, P;
     float scale_log2;
 };
@@ -362,7 +363,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 bool next_box = finish(sl0, next, next_slot0);
                 // store-then-attend: the pool rows this launch reads may have been written by the
                 // preceding store grid (launched ahead with programmatic stream serialisation)
-                grid_dependency_wait();
+                if (p.early_wait) grid_dependency_wait();
                 for (int e = 0; e < n_kv; ++e) {          // ring entries in load order
                     const int s = e % nst;
                     const int j = ks.entry_tile(e);           // the key tile entry e holds
@@ -710,6 +711,13 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+    // A grid chained after this one (the attention of the next layer) may start once every CTA
+    // is here, and this one completes after its own predecessor: the grids of a chain complete
+    // in launch order.  (Releasing the next grid earlier, at the producers' start, filled this
+    // grid's last wave with it, but some such chained launches saw a K stage never fill and ran
+    // a barrier wait out to its budget.)
+    grid_launch_dependents();
+    if (threadIdx.x == 0) grid_dependency_wait();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -918,8 +926,9 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
 }
 
-// pdl: launched with programmatic stream serialisation after a store grid that releases it
-// early (store-then-attend); the producers' grid-dependency wait orders the reads.
+// pdl: launched with programmatic stream serialisation after a grid that releases it early --
+// a store (store-then-attend; prm.early_wait orders the pool reads after it) or the attention
+// of another layer (chained layers; prm.early_wait = 0).
 template <int kMode, bool kDrop = false>
 int launch_attn(const AttnParams& prm, int B, cudaStream_t stream, bool pdl = false) {
     const int64_t ctas = (int64_t)B * prm.Hq * ((prm.n_rows + kQT * kBM - 1) / (kQT * kBM));
@@ -958,7 +967,7 @@ bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == k
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
-                             cudaStream_t stream, bool drop_none, bool pdl) {
+                             cudaStream_t stream, bool drop_none, bool pdl, bool chained) {
     if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
         return ACACHE_ERR_INVALID_ARG;
     AttnParams prm{};
@@ -973,13 +982,14 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     prm.out = (bf16*)out;
     prm.dev_status = dev_status;
     prm.num_slots = num_slots;
+    prm.early_wait = chained ? 0 : 1;
     prm.n_rows = n_q;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
     prm.T_len = T_len;
     prm.scale_log2 = a.scale * kLog2e;
-    return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream, pdl)
-                     : launch_attn<kSlotKeys>(prm, B, stream, pdl);
+    return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream, pdl || chained)
+                     : launch_attn<kSlotKeys>(prm, B, stream, pdl || chained);
 }
 
 int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_start, int max_q,
@@ -1002,6 +1012,7 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
     prm.out = (bf16*)out;
     prm.dev_status = dev_status;
     prm.num_slots = num_slots;
+    prm.early_wait = 1;
     prm.n_rows = max_q;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
@@ -1030,6 +1041,7 @@ int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, co
     prm.stat_m = stat_m;
     prm.stat_l = stat_l;
     prm.dev_status = dev_status;
+    prm.early_wait = 1;
     prm.n_rows = P;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;

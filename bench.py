@@ -180,6 +180,9 @@ class Path:
         self.write_pos = torch.empty((w.batch, w.R), dtype=torch.int32, device=device)
         self.read_slot = torch.empty((w.batch, w.T), dtype=torch.int32, device=device)
         self.out = [torch.empty_like(r["q_r"]) for r in self.rec]
+        self.k_new_l = [r["k_new"] for r in self.rec]
+        self.v_new_l = [r["v_new"] for r in self.rec]
+        self.q_r_l = [r["q_r"] for r in self.rec]
         self.launches_per_step = w.layers * 3 + 2 + w.recompute_points * w.layers * 2
         torch.cuda.synchronize()
 
@@ -210,23 +213,22 @@ class Path:
         ac.acache_build_slot_maps(w.batch, w.T, w.l, w.L, w.K, self.anchors, lay.shared_slot,
                                   lay.private_slots, self.write_pos, self.read_slot)
         for point in range(w.recompute_points):
-            for n in range(w.layers):
-                r = self.rec[n]
-                if e2e and point == 0:
+            if e2e and point == 0:
+                # inputs still arriving: each layer starts as soon as its own upload is in
+                for n in range(w.layers):
+                    r = self.rec[n]
                     s.wait_event(self.ev_rec_ready[n])
-                ac.acache_write_slots(self.desc, w.batch, w.R, lay.private_slots, r["k_new"],
-                                      r["v_new"], self.kc[n], self.vc[n], lay.num_slots,
-                                      lay.private_begin)
-                if ev is not None:
-                    a = torch.cuda.Event(enable_timing=True)
-                    a.record(s)
-                ac.acache_slot_attention(self.desc, w.batch, w.R, r["q_r"], w.T, self.read_slot,
-                                         self.kc[n], self.vc[n], lay.num_slots, self.out[n])
-                if ev is not None:
-                    b = torch.cuda.Event(enable_timing=True)
-                    b.record(s)
-                    ev["slot"].append((a, b))
-                if e2e and point == w.recompute_points - 1:
+                    ac.acache_store_attend(self.desc, w.batch, w.R, lay.private_slots, r["k_new"], r["v_new"],
+                                           self.kc[n], self.vc[n], lay.num_slots, lay.private_begin, w.R,
+                                           r["q_r"], w.T, self.read_slot, self.out[n])
+            else:
+                # one recompute point over all layers in one call: the stores of every layer, then
+                # the attentions, their grids chained
+                ac.acache_store_attend_layers(self.desc, w.batch, w.R, lay.private_slots, self.k_new_l,
+                                              self.v_new_l, self.kc, self.vc, lay.num_slots, lay.private_begin,
+                                              w.R, self.q_r_l, w.T, self.read_slot, self.out)
+            if e2e and point == w.recompute_points - 1:
+                for n in range(w.layers):
                     self.ev_rec_done[n].record(s)
 
     # ---- host buffers for the end-to-end measurement ---------------------------------
@@ -373,6 +375,40 @@ class Decode:
         }
 
 
+def slot_launch_times(path, reps=3):
+    """The read-slot attention of one recompute point over all layers, timed two ways with
+    CUDA events: chained as the step runs it (acache_store_attend_layers with no store, one
+    call; ms per launch = the call / layers), and one launch at a time (events around each
+    acache_slot_attention).  Returns (chained, alone) ms per launch."""
+    ac, w, lay = path.ac, path.w, path.lay
+
+    def chained():
+        ac.acache_store_attend_layers(path.desc, w.batch, 0, None, None, None, path.kc, path.vc, lay.num_slots,
+                                      lay.private_begin, w.R, path.q_r_l, w.T, path.read_slot, path.out)
+
+    chained()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        chained()
+    b.record()
+    torch.cuda.synchronize()
+    t_chain = a.elapsed_time(b) / (reps * w.layers)
+    pairs = []
+    for _ in range(reps):
+        for n in range(w.layers):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ac.acache_slot_attention(path.desc, w.batch, w.R, path.q_r_l[n], w.T, path.read_slot, path.kc[n],
+                                     path.vc[n], lay.num_slots, path.out[n])
+            e1.record()
+            pairs.append((e0, e1))
+    torch.cuda.synchronize()
+    t_alone = statistics.mean(e0.elapsed_time(e1) for e0, e1 in pairs)
+    return t_chain, t_alone
+
+
 def store_attend_compare(path, reps=3):
     """One recompute point over all layers: the store and the attention as two calls, against
     acache_store_attend (one call; the attention grid starts while the store drains).
@@ -392,14 +428,21 @@ def store_attend_compare(path, reps=3):
                 ac.acache_slot_attention(path.desc, w.batch, w.R, r["q_r"], w.T, path.read_slot,
                                          path.kc[n], path.vc[n], lay.num_slots, path.out[n])
 
+    def run_layers():
+        ac.acache_store_attend_layers(path.desc, w.batch, w.R, lay.private_slots, path.k_new_l, path.v_new_l,
+                                      path.kc, path.vc, lay.num_slots, lay.private_begin, w.R, path.q_r_l, w.T,
+                                      path.read_slot, path.out)
+
     res = {}
-    for name, fused in (("separate_ms_per_layer", False), ("store_attend_ms_per_layer", True)):
-        run(fused)
+    for name, fused in (("separate_ms_per_layer", False), ("store_attend_ms_per_layer", True),
+                        ("store_attend_layers_ms_per_layer", None)):
+        fn = run_layers if fused is None else (lambda f=fused: run(f))
+        fn()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(reps):
-            run(fused)
+            fn()
         b.record()
         torch.cuda.synchronize()
         res[name] = a.elapsed_time(b) / (reps * w.layers)
@@ -644,7 +687,7 @@ def main():
     def max_over_ranks(x):
         return reduce_max(x, dev)
 
-    ev = {"select": [], "slot": []}
+    ev = {"select": []}
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv")
                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/acache_clocks_{rank}.csv")
     barrier()
@@ -660,7 +703,7 @@ def main():
     ms = max_over_ranks(start.elapsed_time(end))
     ms_per_step = ms / args.steps
     tflops = step_flops(w) * args.steps * world / (ms / 1e3) / 1e12
-    slot_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["slot"])
+    slot_ms, slot_alone_ms = slot_launch_times(path)
     select_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["select"])
     scored_tok_s = w.batch * w.L / (select_ms / 1e3)
     peaks = measured_peaks()
@@ -715,6 +758,9 @@ def main():
             "anchor_scored_tokens_per_s": scored_tok_s,
             "select_ms": select_ms,
             "slot_attn_ms_per_launch": slot_ms,
+            "slot_attn_timing": "per launch within one call over all layers (launches chained); "
+                                "slot_attn_ms_per_launch_alone: one launch at a time",
+            "slot_attn_ms_per_launch_alone": slot_alone_ms,
             "roofline": {"bound": "tensor", "kernel": "slot_attention", "achieved": slot_achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": slot_achieved / peak,
                          "peak_source": f"{peaks['source']} bf16 sustained", "traffic": traffic},

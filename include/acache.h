@@ -238,6 +238,31 @@ ACACHE_API int acache_slot_attention(const acache_attn_desc* a, int batch, int n
                           int32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * (4a') Store-then-attend over the layers of one recompute point.  Page: Sec. 4.3 and
+ * App. C.1 (each layer stores its recomputed rows, then attends through the read-slot map).
+ * The computation of acache_store_attend for layer 0, 1, ..., layers-1 in that order on
+ * the stream.  Per-layer buffers are passed as arrays of `layers` DEVICE pointers; the
+ * arrays themselves are in HOST memory and are read during the call only:
+ *   k_new, v_new   [layers] -> [B][rows][Hkv][d]      (ignored when rows = 0)
+ *   k_cache, v_cache [layers] -> [num_slots][Hkv][d] (one pool per layer)
+ *   q, out         [layers] -> [B][n_q][Hq][d]       (ignored when n_q = 0)
+ * write_slot [B][rows] and read_slot [B][T] are shared by all layers.
+ * When no layer's pools or output overlap any buffer of another layer (checked on the host),
+ * the grids are chained with programmatic dependent launch: the stores of all layers run
+ * back to back, then -- once they are complete -- the attentions (tensor-core path), each
+ * starting on the SMs its predecessor's last wave leaves idle; work enqueued on the stream
+ * after the call runs after all of them.  Otherwise -- or on the CUDA-core and
+ * block-decode paths -- the layers run one after the other.  Every argument of every layer
+ * is checked before anything is launched; errors as acache_store_attend.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_store_attend_layers(const acache_attn_desc* a, int layers, int batch,
+                        int rows, const int32_t* write_slot, const void* const* k_new,
+                        const void* const* v_new, void* const* k_cache, void* const* v_cache,
+                        int64_t num_slots, int64_t private_begin, int n_q, const void* const* q,
+                        int seq_len, const int32_t* read_slot, void* const* out,
+                        int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * (4b') Read-slot attention with discarded keys -- the DropNA ablation.  Page: Sec. 5.3
  * (Figure 5) and App. B.4: the same anchors are recomputed, but every non-anchor affix
  * entry of the cache is discarded instead of read from the shared region.

@@ -136,3 +136,75 @@ def test_store_attend_one_half_only():
     torch.cuda.synchronize()
     ref = oracle.slot_attention(q.cpu(), rs.cpu(), kc.cpu(), vc.cpu(), scale=d ** -0.5)
     assert_out_close(o.double().cpu().numpy(), ref, "bf16", "attend only")
+
+
+# ----------------------------------------------------------- store-then-attend over layers
+def _layers_case(L, B, rows, n_q, hq, hkv, T, d, ns, priv0, seed):
+    g = torch.Generator().manual_seed(seed)
+    dt = torch.bfloat16
+    kc = [torch.randn((ns, hkv, d), generator=g).to(dt) for _ in range(L)]
+    vc = [torch.randn((ns, hkv, d), generator=g).to(dt) for _ in range(L)]
+    ws = (priv0 + torch.randperm(ns - priv0, generator=g)[:B * rows]).to(torch.int32).reshape(B, rows)
+    rs = torch.randint(0, priv0, (B, T), generator=g, dtype=torch.int32)
+    for b in range(B):
+        pos = torch.randperm(T, generator=g)[:min(rows, T)]
+        rs[b, pos] = ws[b, :len(pos)]
+    kn = [torch.randn((B, rows, hkv, d), generator=g).to(dt) for _ in range(L)]
+    vn = [torch.randn((B, rows, hkv, d), generator=g).to(dt) for _ in range(L)]
+    q = [(torch.randn((B, n_q, hq, d), generator=g) * 2).to(dt) for _ in range(L)]
+    return kc, vc, ws, rs, kn, vn, q
+
+
+@pytest.mark.parametrize("L,B,rows,n_q,T", [(3, 2, 300, 300, 700), (4, 1, 40, 40, 1408), (2, 3, 0, 129, 300),
+                                            (3, 2, 77, 0, 300)])
+def test_store_attend_layers_equals_per_layer_calls(L, B, rows, n_q, T):
+    hq, hkv, d, ns, priv0 = 4, 2, 128, 3000, 1000
+    kc, vc, ws, rs, kn, vn, q = _layers_case(L, B, rows, n_q, hq, hkv, T, d, ns, priv0, seed=L * 10 + rows)
+    desc = ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # one call over all layers (chained grids)
+    k1, v1 = [dev(x) for x in kc], [dev(x) for x in vc]
+    o1 = [torch.empty((B, n_q, hq, d), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ac.acache_store_attend_layers(desc, B, rows, dev(ws), [dev(x) for x in kn] if rows else None,
+                                  [dev(x) for x in vn] if rows else None, k1, v1, ns, priv0, n_q,
+                                  [dev(x) for x in q] if n_q else None, T, dev(rs), o1 if n_q else None,
+                                  dev_status=st)
+    # one call per layer
+    k2, v2 = [dev(x) for x in kc], [dev(x) for x in vc]
+    o2 = [torch.empty_like(o) for o in o1]
+    for l in range(L):
+        ac.acache_store_attend(desc, B, rows, dev(ws), dev(kn[l]) if rows else None, dev(vn[l]) if rows else None,
+                               k2[l], v2[l], ns, priv0, n_q, dev(q[l]) if n_q else None, T, dev(rs),
+                               o2[l] if n_q else None, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for l in range(L):
+        assert torch.equal(k1[l], k2[l]) and torch.equal(v1[l], v2[l]), f"pool of layer {l}"
+        if n_q:
+            assert torch.equal(o1[l], o2[l]), f"output of layer {l}"
+    if n_q:
+        ref = oracle.slot_attention(q[L - 1], rs, k1[L - 1].cpu(), v1[L - 1].cpu(), scale=d ** -0.5)
+        assert_out_close(o1[L - 1].double().cpu().numpy(), ref, "bf16", "last layer")
+
+
+def test_store_attend_layers_shared_pool_runs_in_order():
+    # two layers on the same pool: the call must behave as the per-layer calls in order (the
+    # second store lands after the first attention has read the pool)
+    L, B, rows, n_q, T, hq, hkv, d, ns, priv0 = 2, 2, 100, 100, 400, 2, 2, 128, 1500, 500
+    kc, vc, ws, rs, kn, vn, q = _layers_case(L, B, rows, n_q, hq, hkv, T, d, ns, priv0, seed=5)
+    desc = ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kp, vp = dev(kc[0]), dev(vc[0])
+    o1 = [torch.empty((B, n_q, hq, d), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ac.acache_store_attend_layers(desc, B, rows, dev(ws), [dev(x) for x in kn], [dev(x) for x in vn], [kp, kp],
+                                  [vp, vp], ns, priv0, n_q, [dev(x) for x in q], T, dev(rs), o1, dev_status=st)
+    kp2, vp2 = dev(kc[0]), dev(vc[0])
+    o2 = [torch.empty_like(o) for o in o1]
+    for l in range(L):
+        ac.acache_store_attend(desc, B, rows, dev(ws), dev(kn[l]), dev(vn[l]), kp2, vp2, ns, priv0, n_q, dev(q[l]),
+                               T, dev(rs), o2[l], dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(kp, kp2) and torch.equal(vp, vp2)
+    for l in range(L):
+        assert torch.equal(o1[l], o2[l])
