@@ -335,7 +335,7 @@ int acache_store_attend_layers(const acache_attn_desc* desc, int layers, int bat
     // Chained: the stores of every layer back to back, then the attentions; each grid may start
     // on the SMs its predecessor's last wave leaves idle.  The first attention is an ordinary
     // launch, so it starts after every store of the call (and every earlier grid) is complete;
-    // the attentions chained after it start only once all of its CTAs are running.
+    // the attentions chained after it start only once all of its CTAs have started reading.
     if (store)
         for (int l = 0; l < layers; ++l)
             if (int rc = launch_write_slots(batch, rows, write_slot, k_new[l], v_new[l], k_cache[l], v_cache[l],
@@ -344,7 +344,7 @@ int acache_store_attend_layers(const acache_attn_desc* desc, int layers, int bat
     if (attend)
         for (int l = 0; l < layers; ++l)
             if (int rc = launch_tc_slot_attention(a, batch, n_q, q[l], seq_len, read_slot, k_cache[l], v_cache[l],
-                                                  num_slots, out[l], dev_status, st, false, false, l > 0))
+                                                  num_slots, out[l], dev_status, st, false, false, l == 0 ? 1 : 2))
                 return rc;
     return ACACHE_OK;
 }

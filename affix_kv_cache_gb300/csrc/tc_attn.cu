@@ -104,6 +104,7 @@ struct AttnParams {
     int32_t* dev_status;
     int64_t num_slots;
     int early_wait;       // 1: the pool may have been written by the grid this one follows
+    int allow_split;      // 0: no split keys (a grid of a chain, which runs beside its successor)
     int n_rows, Hq, Hkv, T_len, L, P;
     float scale_log2;
 };
@@ -240,7 +241,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     const int n_qt = min(kQT, (n_rows - q0 + kBM - 1) / kBM);   // Q tiles present (1 or 2)
     const int n_kv = n_key_tiles<kMode>(p, T_len);
     // one Q tile and at least two key tiles: split the keys between the two chains
-    const bool split = n_qt == 1 && n_kv >= 2;
+    const bool split = p.allow_split && n_qt == 1 && n_kv >= 2;
     const int n_ch = split ? 2 : n_qt;                  // chains: softmax warpgroups, MMA threads
     const KeySchedule ks{split, n_kv, split ? (n_kv + 1) / 2 : n_kv};
     // with split keys the second Q buffer is free and serves as a third V stage
@@ -362,8 +363,12 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 int next[4], next_slot0;
                 bool next_box = finish(sl0, next, next_slot0);
                 // store-then-attend: the pool rows this launch reads may have been written by the
-                // preceding store grid (launched ahead with programmatic stream serialisation)
+                // preceding store grid (launched ahead with programmatic stream serialisation).
+                // Only then may the next grid on the stream start: in a chain of layers it runs on
+                // the SMs this grid's last wave leaves idle, and reads its own layer's pool
+                // without waiting (that store is complete once this wait returns).
                 if (p.early_wait) grid_dependency_wait();
+                grid_launch_dependents();
                 for (int e = 0; e < n_kv; ++e) {          // ring entries in load order
                     const int s = e % nst;
                     const int j = ks.entry_tile(e);           // the key tile entry e holds
@@ -711,13 +716,6 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-    // A grid chained after this one (the attention of the next layer) may start once every CTA
-    // is here, and this one completes after its own predecessor: the grids of a chain complete
-    // in launch order.  (Releasing the next grid earlier, at the producers' start, filled this
-    // grid's last wave with it, but some such chained launches saw a K stage never fill and ran
-    // a barrier wait out to its budget.)
-    grid_launch_dependents();
-    if (threadIdx.x == 0) grid_dependency_wait();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -967,7 +965,7 @@ bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == k
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
-                             cudaStream_t stream, bool drop_none, bool pdl, bool chained) {
+                             cudaStream_t stream, bool drop_none, bool pdl, int chain_pos) {
     if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
         return ACACHE_ERR_INVALID_ARG;
     AttnParams prm{};
@@ -982,7 +980,13 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     prm.out = (bf16*)out;
     prm.dev_status = dev_status;
     prm.num_slots = num_slots;
+    // chain_pos: 0 a single launch, 1 the first grid of a chain of layers, 2 a later one
+    const bool chained = chain_pos == 2;
     prm.early_wait = chained ? 0 : 1;
+    // A split-key CTA with tiled box loads, running beside the next grid of a chain, sometimes
+    // saw a K stage never fill (a barrier wait ran out its budget); the grids of a chain do not
+    // split (their successor fills the last wave instead).
+    prm.allow_split = chain_pos == 0 ? 1 : 0;
     prm.n_rows = n_q;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
@@ -1013,6 +1017,7 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
     prm.dev_status = dev_status;
     prm.num_slots = num_slots;
     prm.early_wait = 1;
+    prm.allow_split = 1;
     prm.n_rows = max_q;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
@@ -1042,6 +1047,7 @@ int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, co
     prm.stat_l = stat_l;
     prm.dev_status = dev_status;
     prm.early_wait = 1;
+    prm.allow_split = 1;
     prm.n_rows = P;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
