@@ -344,7 +344,7 @@ int acache_store_attend_layers(const acache_attn_desc* desc, int layers, int bat
     if (attend)
         for (int l = 0; l < layers; ++l)
             if (int rc = launch_tc_slot_attention(a, batch, n_q, q[l], seq_len, read_slot, k_cache[l], v_cache[l],
-                                                  num_slots, out[l], dev_status, st, false, false, l == 0 ? 1 : 2))
+                                                  num_slots, out[l], dev_status, st, false, false, l > 0))
                 return rc;
     return ACACHE_OK;
 }

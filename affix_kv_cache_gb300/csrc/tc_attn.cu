@@ -104,7 +104,6 @@ struct AttnParams {
     int32_t* dev_status;
     int64_t num_slots;
     int early_wait;       // 1: the pool may have been written by the grid this one follows
-    int allow_split;      // 0: no split keys (a grid of a chain, which runs beside its successor)
     int n_rows, Hq, Hkv, T_len, L, P;
     float scale_log2;
 };
@@ -241,7 +240,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     const int n_qt = min(kQT, (n_rows - q0 + kBM - 1) / kBM);   // Q tiles present (1 or 2)
     const int n_kv = n_key_tiles<kMode>(p, T_len);
     // one Q tile and at least two key tiles: split the keys between the two chains
-    const bool split = p.allow_split && n_qt == 1 && n_kv >= 2;
+    const bool split = n_qt == 1 && n_kv >= 2;
     const int n_ch = split ? 2 : n_qt;                  // chains: softmax warpgroups, MMA threads
     const KeySchedule ks{split, n_kv, split ? (n_kv + 1) / 2 : n_kv};
     // with split keys the second Q buffer is free and serves as a third V stage
@@ -259,17 +258,19 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     if (kMode == kSlotKeys && prod_warp)
         tile_slots<kDrop>(p, kbase, T_len, n_kv, ks.entry_tile(0), lane, flagger, sl0);
 
+    // read-slot K/V stages: one arrival per warp of the producer trio (see the producers)
+    constexpr int kFullArrivals = kMode == kSlotKeys ? 3 : 1;
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 1);
         // a K or V stage is free once every chain that reads its entry is done with it (both
         // Q tiles' chains; with split keys the one chain the entry belongs to)
         const int readers = split ? 1 : n_qt;
         for (int s = 0; s < kKStages; ++s) {
-            mbar_init(&ctl.k_full[s], 1);
+            mbar_init(&ctl.k_full[s], kFullArrivals);
             mbar_init(&ctl.k_empty[s], readers);
         }
         for (int s = 0; s < kVStages + 1; ++s) {
-            mbar_init(&ctl.v_full[s], 1);
+            mbar_init(&ctl.v_full[s], kFullArrivals);
             mbar_init(&ctl.v_empty[s], readers);
         }
         for (int t = 0; t < kQT; ++t) {
@@ -381,9 +382,16 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                         !__all_sync(0xffffffffu, wait_bar(&empty[s], ((e / nst) - 1) & 1, abort_flag,
                                                           dev_status)))
                         break;
-                    // the trio's first warp announces the tile's bytes; a gather of another warp
-                    // that completes first leaves the count transiently negative (allowed)
+                    // The trio's first warp announces the tile's bytes; a gather of another warp
+                    // that completes first leaves the count transiently negative (allowed).  Read-
+                    // slot stages count one arrival per warp of the trio, also for a box tile that
+                    // the first warp loads alone: no stage then completes a phase without every
+                    // warp, so none can fall two phases behind a barrier or get ahead of it -- a
+                    // parity wait cannot tell two completed phases from none.  (Without this, a box
+                    // tile of split keys, whose chain runs ahead of the other, could be released
+                    // twice before a warp busy with the other chain's gathers looked at its stage.)
                     if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
+                    else if (kMode == kSlotKeys && lane == 0) mbar_arrive(&full[s]);
                     __syncwarp();
                     if (kMode == kSlotKeys) {
                         if (box) {
@@ -965,7 +973,7 @@ bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == k
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
-                             cudaStream_t stream, bool drop_none, bool pdl, int chain_pos) {
+                             cudaStream_t stream, bool drop_none, bool pdl, bool chained) {
     if ((int64_t)num_slots * a.hkv >= 0x7fffffffLL || (int64_t)B * n_q >= 0x7fffffffLL)
         return ACACHE_ERR_INVALID_ARG;
     AttnParams prm{};
@@ -980,13 +988,9 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     prm.out = (bf16*)out;
     prm.dev_status = dev_status;
     prm.num_slots = num_slots;
-    // chain_pos: 0 a single launch, 1 the first grid of a chain of layers, 2 a later one
-    const bool chained = chain_pos == 2;
+    // chained: a later grid of a chain of layers, launched behind the previous layer's
+    // attention; it reads only its own layer's pool, complete before the chain's first grid
     prm.early_wait = chained ? 0 : 1;
-    // A split-key CTA with tiled box loads, running beside the next grid of a chain, sometimes
-    // saw a K stage never fill (a barrier wait ran out its budget); the grids of a chain do not
-    // split (their successor fills the last wave instead).
-    prm.allow_split = chain_pos == 0 ? 1 : 0;
     prm.n_rows = n_q;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
@@ -1017,7 +1021,6 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
     prm.dev_status = dev_status;
     prm.num_slots = num_slots;
     prm.early_wait = 1;
-    prm.allow_split = 1;
     prm.n_rows = max_q;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
@@ -1047,7 +1050,6 @@ int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, co
     prm.stat_l = stat_l;
     prm.dev_status = dev_status;
     prm.early_wait = 1;
-    prm.allow_split = 1;
     prm.n_rows = P;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;

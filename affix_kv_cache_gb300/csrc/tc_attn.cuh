@@ -23,7 +23,7 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
                              int64_t num_slots, void* out, int32_t* dev_status,
                              cudaStream_t stream, bool drop_none = false, bool pdl = false,
-                             int chain_pos = 0);
+                             bool chained = false);
 // Ragged batches: request b's query rows are [q_start[b], q_start[b+1]) of q / out
 // ([total_q][Hq][d]) and its logical keys read_slot[kv_start[b] .. kv_start[b+1]); max_q and
 // max_T bound the per-request counts (a request outside them is skipped and flagged).

@@ -280,6 +280,24 @@ class Path:
         self.h_out.copy_(self.out[-1], non_blocking=True)
         s.wait_stream(cs)
 
+    def upload_ms(self, reps=3):
+        """Milliseconds to upload one step's inputs with nothing else running: the host link's
+        share of the end-to-end step (the link is shared with the box's other GPUs)."""
+        cs = self.copy_stream
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cs)
+        with torch.cuda.stream(cs):
+            for _ in range(reps):
+                for n in range(self.w.layers):
+                    for k, v in self.h_probe[n].items():
+                        self.probe[n][k].copy_(v, non_blocking=True)
+                    for k, v in self.h_rec[n].items():
+                        self.rec[n][k].copy_(v, non_blocking=True)
+        z.record(cs)
+        torch.cuda.synchronize()
+        return a.elapsed_time(z) / reps
+
 
 class Decode:
     """Block-decode steps on a Path's pools: per layer, the current block's fresh K/V are
@@ -714,7 +732,9 @@ def main():
     e2e = None
     if not args.no_e2e:
         bi, bo = path.host_inputs()
-        path.step_e2e()
+        up_ms = path.upload_ms()
+        for _ in range(2):
+            path.step_e2e()
         torch.cuda.synchronize()
         barrier()
         e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -729,7 +749,8 @@ def main():
         ems = max_over_ranks(e_s.elapsed_time(e_e))
         e2e = {"value": step_flops(w) * n_e2e * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "ms_per_step": ems / n_e2e}
+               "ms_per_step": ems / n_e2e, "upload_ms_per_step": up_ms,
+               "h2d_gbs": bi / (up_ms / 1e3) / 1e9}
 
     decode = None
     if not args.no_decode:
