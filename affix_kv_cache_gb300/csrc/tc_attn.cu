@@ -7,7 +7,7 @@
 //
 // tc_attn_kernel  (probe forward and read-slot attention at a recompute point; one CTA per
 //                  256 query rows -- two 128-row Q tiles A and B -- of one (request, query
-//                  head); 512 threads in four warpgroups, 1 CTA per SM)
+//                  head); 640 threads in five warpgroups, 1 CTA per SM)
 //   WG0, WG1  softmax + epilogue of tile A / B: thread r owns query row r (= TMEM lane r).
 //             Per key tile j: read S_t(j) from TMEM, row maximum, exponentiate in base 2
 //             against a lazily raised maximum (it only moves when it grows by more than 2^8;
@@ -20,16 +20,16 @@
 //             S_t(j) = Q_t K_j^T (SS, M = N = 128) and O_t += P_t(j) V_j (TS: P from TMEM,
 //             V an MN-major shared-memory operand), S_t(j+1) right after PV_t(j).  Warps 10
 //             and 11 are TMA producers.
-//   WG3       TMA producers: warps 12, 13 and 10 fill a 3-stage K ring, warps 14, 15 and 11 a
-//             2-stage V ring.  Read-slot keys: a tile whose 128 slots are consecutive (a
-//             request's own rows, a page of the shared region) is two tiled box loads of the
-//             pool; any other is 64 `tile::gather4` loads (4 pool rows x 64 columns, rows
-//             resolved through the read-slot map one tile ahead), about 21 per warp -- each
-//             gather4 a lane issues costs its warp tens of cycles, so the gather rate grows
-//             with the number of issuing warps.  Probe keys: the affix rows
-//             and the request's own rows are contiguous per KV head, so a tile is two tiled
-//             box loads.  Loads complete on the stage's mbarrier by byte count.
-//   setmaxnreg gives the softmax warpgroups 200 registers and WG2 / WG3 56.
+//   WG3, WG4  TMA producers: warps 10-14 fill a 3-stage K ring, warps 15-19 a 2-stage V
+//             ring.  Read-slot keys: a tile whose 128 slots are consecutive (a request's own
+//             rows, a page of the shared region) is two tiled box loads of the pool; any other
+//             is 64 `tile::gather4` loads (4 pool rows x 64 columns, rows resolved through the
+//             read-slot map one tile ahead), 12-13 per warp -- each gather4 a lane issues costs
+//             its warp tens of cycles, so the gather rate grows with the number of issuing
+//             warps.  Probe keys: the affix rows and the request's own rows are contiguous per
+//             KV head, so a tile is two tiled box loads.  Loads complete on the stage's
+//             mbarrier by byte count.
+//   setmaxnreg gives the softmax warpgroups 168 registers and WG2-WG4 48.
 //   A CTA left with one Q tile (the ragged last query block) splits its keys instead: chain A
 //   takes the first half of the key tiles and chain B the second half, both against the same
 //   Q tile, so the two chains still ping-pong; the K/V rings then alternate A's and B's tiles,
@@ -69,14 +69,15 @@ constexpr int kKStages = 3;                 // K ring: a K tile is free once S_B
 constexpr int kVStages = 2;                 // V ring: a V tile is free once PV_B has read it
 constexpr int kMmaWarp = 8;                 // warpgroup 2: TMEM allocation; warps 8 and 9 each
                                             // issue the MMAs of one Q tile
-constexpr int kProdWarp = 12;               // warpgroup 3: TMA producer warps (joined by the
-constexpr int kProdWarps = 4;               // idle warps 10 and 11 of warpgroup 2)
-constexpr int kThreads = 16 * 32;
-static_assert(kThreads == (kProdWarp + kProdWarps) * 32, "warp roles");
-// Registers: 512 threads x 128 at launch = 65536; the softmax warpgroups grow to 200, the
-// MMA / producer warpgroups shrink to 56: 2*128*200 + 2*128*56 = 65536.
-constexpr int kRegSoftmax = 200, kRegOther = 56;
-static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther <= kThreads * 128, "register split");
+constexpr int kProdWarp = 10;               // first TMA producer warp
+constexpr int kProdPerRing = 5;             // producer warps per ring: K warps 10-14, V 15-19
+constexpr int kThreads = (kProdWarp + 2 * kProdPerRing) * 32;
+static_assert(kThreads % 128 == 0, "whole warpgroups");
+// Registers: 640 threads x 96 at launch = 61440; the softmax warpgroups grow to 168, the MMA /
+// producer warpgroups shrink to 48: 2*128*168 + 3*128*48 = 61440 (no spills).
+constexpr int kRegLaunch = 65536 / kThreads / 8 * 8;
+constexpr int kRegSoftmax = 168, kRegOther = 48;
+static_assert(2 * 128 * kRegSoftmax + (kThreads - 256) * kRegOther <= kThreads * kRegLaunch, "register split");
 constexpr uint32_t kTileBytes = kBN * kD * 2;     // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t kRegion = kBN * 128;           // 16 KB: 64 columns of a 128-row tile
 constexpr uint32_t kSmemBytes = kTileBytes * (kQT + kKStages + kVStages) + 1024;
@@ -258,8 +259,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     if (kMode == kSlotKeys && prod_warp)
         tile_slots<kDrop>(p, kbase, T_len, n_kv, ks.entry_tile(0), lane, flagger, sl0);
 
-    // read-slot K/V stages: one arrival per warp of the producer trio (see the producers)
-    constexpr int kFullArrivals = kMode == kSlotKeys ? 3 : 1;
+    // read-slot K/V stages: one arrival per producer warp of the ring (see the producers)
+    constexpr int kFullArrivals = kMode == kSlotKeys ? kProdPerRing : 1;
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 1);
         // a K or V stage is free once every chain that reads its entry is done with it (both
@@ -318,11 +319,11 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 tma_prefetch_desc(&p.tm_k1);
                 tma_prefetch_desc(&p.tm_v1);
             }
-            // warps 12, 13 and 10 fill the K ring, warps 14, 15 and 11 the V ring (a gather4 costs
-            // its warp tens of cycles of issue, so the tile's 64 are spread over three warps); probe
-            // tiles are box loads issued by lane 0 of warps 12 (K) and 14 (V)
-            const bool is_v = warp == kMmaWarp + 3 || warp >= kProdWarp + 2;
-            const int pi = warp >= kProdWarp ? (warp - kProdWarp) & 1 : 2;   // place in the ring's trio
+            // kProdPerRing warps fill the K ring, as many the V ring (a gather4 costs its warp tens
+            // of cycles of issue, so a tile's 64 are spread over the ring's warps); probe tiles are
+            // box loads issued by lane 0 of each ring's first warp
+            const bool is_v = warp >= kProdWarp + kProdPerRing;
+            const int pi = warp - kProdWarp - (is_v ? kProdPerRing : 0);    // place among the ring's warps
             const int nst = is_v ? n_vst : kKStages;
             uint64_t* full = is_v ? ctl.v_full : ctl.k_full;
             uint64_t* empty = is_v ? ctl.v_empty : ctl.k_empty;
@@ -333,8 +334,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 const int n_aff = (p.L + kBN - 1) / kBN;
                 const int oob_row = (int)(p.num_slots * p.Hkv);     // first row outside the pool
                 // read-slot keys: this lane's gather x = 4-row group x / 2 of the tile, column
-                // half x % 2 of the trio's matrix (K or V); lanes with x >= 64 have none
-                const int x = 3 * lane + pi;
+                // half x % 2 of the ring's matrix (K or V); lanes with x >= 64 have none
+                const int x = kProdPerRing * lane + pi;
                 const bool gathers = x < 64;
                 const int g = x >> 1, half = x & 1;
                 // Read-slot tile j, resolved one entry ahead (the loads overlap the previous tile's
@@ -342,7 +343,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 // whether all 128 keys are present with consecutive slots (a request's own rows, a
                 // page of the shared region) -- then the tile is two tiled box loads of the pool
                 // (slot0 = the first slot), else 64 gather4 loads whose rows each lane takes from
-                // the lane that read them.  Every warp of the trio reads the same slots and so
+                // the lane that read them.  Every warp of the ring reads the same slots and so
                 // takes the same decision.  Invalid slots and keys past T read an out-of-range row.
                 auto finish = [&](const int (&sl)[4], int (&rows)[4], int& slot0) -> bool {
                     bool run = sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 && sl[3] == sl[0] + 3;
@@ -382,9 +383,9 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                         !__all_sync(0xffffffffu, wait_bar(&empty[s], ((e / nst) - 1) & 1, abort_flag,
                                                           dev_status)))
                         break;
-                    // The trio's first warp announces the tile's bytes; a gather of another warp
+                    // The ring's first warp announces the tile's bytes; a gather of another warp
                     // that completes first leaves the count transiently negative (allowed).  Read-
-                    // slot stages count one arrival per warp of the trio, also for a box tile that
+                    // slot stages count one arrival per warp of the ring, also for a box tile that
                     // the first warp loads alone: no stage then completes a phase without every
                     // warp, so none can fall two phases behind a barrier or get ahead of it -- a
                     // parity wait cannot tell two completed phases from none.  (Without this, a box

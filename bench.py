@@ -186,10 +186,8 @@ class Path:
         self.launches_per_step = w.layers * 3 + 2 + w.recompute_points * w.layers * 2
         torch.cuda.synchronize()
 
-    def step(self, ev=None, e2e=False):
-        """One pass of the path.  `ev` (optional) collects CUDA events around phases; with
-        `e2e` the step waits for each layer's uploaded inputs and records when it is done
-        with them (see step_e2e)."""
+    def step(self, ev=None):
+        """One pass of the path.  `ev` (optional) collects CUDA events around phases."""
         ac, w, lay = self.ac, self.w, self.lay
         s = torch.cuda.current_stream()
         self.scores.zero_()
@@ -198,13 +196,9 @@ class Path:
             e0.record(s)
         for n in range(w.layers):
             p = self.probe[n]
-            if e2e:
-                s.wait_event(self.ev_probe_ready[n])
             ac.acache_probe_scores(self.desc, w.batch, w.T, w.l, w.L, self.masked, w.m, p["q"],
                                    p["k_req"], p["v_req"], p["k_aff"], p["v_aff"], self.probe_out,
                                    self.scores, self.ws, self.ws_bytes)
-            if e2e:
-                self.ev_probe_done[n].record(s)
         ac.acache_topk_anchors(self.scores, w.batch, w.L, w.K, self.anchors)
         if ev is not None:
             e1 = torch.cuda.Event(enable_timing=True)
@@ -212,30 +206,23 @@ class Path:
             ev["select"].append((e0, e1))
         ac.acache_build_slot_maps(w.batch, w.T, w.l, w.L, w.K, self.anchors, lay.shared_slot,
                                   lay.private_slots, self.write_pos, self.read_slot)
-        for point in range(w.recompute_points):
-            if e2e and point == 0:
-                # inputs still arriving: each layer starts as soon as its own upload is in
-                for n in range(w.layers):
-                    r = self.rec[n]
-                    s.wait_event(self.ev_rec_ready[n])
-                    ac.acache_store_attend(self.desc, w.batch, w.R, lay.private_slots, r["k_new"], r["v_new"],
-                                           self.kc[n], self.vc[n], lay.num_slots, lay.private_begin, w.R,
-                                           r["q_r"], w.T, self.read_slot, self.out[n])
-            else:
-                # one recompute point over all layers in one call: the stores of every layer, then
-                # the attentions, their grids chained
-                ac.acache_store_attend_layers(self.desc, w.batch, w.R, lay.private_slots, self.k_new_l,
-                                              self.v_new_l, self.kc, self.vc, lay.num_slots, lay.private_begin,
-                                              w.R, self.q_r_l, w.T, self.read_slot, self.out)
-            if e2e and point == w.recompute_points - 1:
-                for n in range(w.layers):
-                    self.ev_rec_done[n].record(s)
+        for _ in range(w.recompute_points):
+            # one recompute point over all layers in one call: the stores of every layer, then
+            # the attentions, their grids chained
+            ac.acache_store_attend_layers(self.desc, w.batch, w.R, lay.private_slots, self.k_new_l,
+                                          self.v_new_l, self.kc, self.vc, lay.num_slots, lay.private_begin,
+                                          w.R, self.q_r_l, w.T, self.read_slot, self.out)
 
     # ---- host buffers for the end-to-end measurement ---------------------------------
+    UPLOADED = ("q", "k_req", "v_req")     # probe inputs a step takes from the host (the affix
+                                          # K/V is the resident shared cache)
+
     def host_inputs(self):
+        """Pinned host copies of every input a step takes from the host, and a second set of
+        device input buffers: step k computes on set k % 2 while step k+1's inputs upload
+        into the other set on a copy stream."""
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-        self.h_probe = [{k: pin(v) for k, v in p.items() if k in ("q", "k_req", "v_req")}
-                        for p in self.probe]
+        self.h_probe = [{k: pin(p[k]) for k in self.UPLOADED} for p in self.probe]
         self.h_rec = [{k: pin(v) for k, v in r.items()} for r in self.rec]
         self.h_anchors = torch.empty(self.anchors.shape, dtype=torch.int32).pin_memory()
         self.h_scores = torch.empty(self.scores.shape, dtype=torch.float32).pin_memory()
@@ -243,58 +230,61 @@ class Path:
         bi = sum(t.numel() * t.element_size() for p in self.h_probe for t in p.values())
         bi += sum(t.numel() * t.element_size() for r in self.h_rec for t in r.values())
         bo = sum(t.numel() * t.element_size() for t in (self.h_anchors, self.h_scores, self.h_out))
+        second_probe = [dict(p, **{k: torch.empty_like(p[k]) for k in self.UPLOADED}) for p in self.probe]
+        second_rec = [{k: torch.empty_like(v) for k, v in r.items()} for r in self.rec]
+        self.sets = [(self.probe, self.rec), (second_probe, second_rec)]
         self.copy_stream = torch.cuda.Stream()
-        L = self.w.layers
-        self.ev_probe_done = [torch.cuda.Event() for _ in range(L)]
-        self.ev_probe_ready = [torch.cuda.Event() for _ in range(L)]
-        self.ev_rec_done = [torch.cuda.Event() for _ in range(L)]
-        self.ev_rec_ready = [torch.cuda.Event() for _ in range(L)]
-        for e in self.ev_probe_done + self.ev_rec_done:   # nothing to wait for before the first step
+        self.ev_ready = [torch.cuda.Event(), torch.cuda.Event()]   # a set's inputs are uploaded
+        self.ev_used = [torch.cuda.Event(), torch.cuda.Event()]    # a set's step is done with them
+        for e in self.ev_used:
             e.record()
         return bi, bo
 
-    def step_e2e(self):
-        """One step end to end: every input of the step is copied from pinned host memory and
-        the step's results (scores, anchors, the last layer's attention output) are read
-        back.  The copies run on their own stream, layer by layer, gated by events, so the
-        next step's inputs upload while the current step computes: a layer's probe inputs as
-        soon as its probe has run, its recompute inputs once the last recompute point has
-        read them."""
-        w, s = self.w, torch.cuda.current_stream()
+    def use_set(self, i):
+        self.probe, self.rec = self.sets[i]
+        self.k_new_l = [r["k_new"] for r in self.rec]
+        self.v_new_l = [r["v_new"] for r in self.rec]
+        self.q_r_l = [r["q_r"] for r in self.rec]
+
+    def upload(self, i):
+        """Copy a step's inputs from pinned host memory into device set i (copy stream), once
+        the step that last used set i is done with it."""
         cs = self.copy_stream
-        for n in range(w.layers):
-            cs.wait_event(self.ev_probe_done[n])
-            with torch.cuda.stream(cs):
+        cs.wait_event(self.ev_used[i])
+        probe, rec = self.sets[i]
+        with torch.cuda.stream(cs):
+            for n in range(self.w.layers):
                 for k, v in self.h_probe[n].items():
-                    self.probe[n][k].copy_(v, non_blocking=True)
-            self.ev_probe_ready[n].record(cs)
-        for n in range(w.layers):
-            cs.wait_event(self.ev_rec_done[n])
-            with torch.cuda.stream(cs):
+                    probe[n][k].copy_(v, non_blocking=True)
                 for k, v in self.h_rec[n].items():
-                    self.rec[n][k].copy_(v, non_blocking=True)
-            self.ev_rec_ready[n].record(cs)
-        self.step(e2e=True)
+                    rec[n][k].copy_(v, non_blocking=True)
+        self.ev_ready[i].record(cs)
+
+    def step_e2e(self, k, upload_next=True):
+        """Step k end to end: it waits for its inputs (uploaded into set k % 2), computes on
+        them and reads its results back (scores, anchors, the last layer's attention output)
+        into pinned host memory; meanwhile the next step's inputs upload into the other set."""
+        s = torch.cuda.current_stream()
+        cur = k % 2
+        if upload_next:
+            self.upload(1 - cur)
+        s.wait_event(self.ev_ready[cur])
+        self.use_set(cur)
+        self.step()
+        self.ev_used[cur].record(s)
         self.h_anchors.copy_(self.anchors, non_blocking=True)
         self.h_scores.copy_(self.scores, non_blocking=True)
         self.h_out.copy_(self.out[-1], non_blocking=True)
-        s.wait_stream(cs)
 
     def upload_ms(self, reps=3):
         """Milliseconds to upload one step's inputs with nothing else running: the host link's
         share of the end-to-end step (the link is shared with the box's other GPUs)."""
-        cs = self.copy_stream
         torch.cuda.synchronize()
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(cs)
-        with torch.cuda.stream(cs):
-            for _ in range(reps):
-                for n in range(self.w.layers):
-                    for k, v in self.h_probe[n].items():
-                        self.probe[n][k].copy_(v, non_blocking=True)
-                    for k, v in self.h_rec[n].items():
-                        self.rec[n][k].copy_(v, non_blocking=True)
-        z.record(cs)
+        a.record(self.copy_stream)
+        for _ in range(reps):
+            self.upload(0)
+        z.record(self.copy_stream)
         torch.cuda.synchronize()
         return a.elapsed_time(z) / reps
 
@@ -733,24 +723,32 @@ def main():
     if not args.no_e2e:
         bi, bo = path.host_inputs()
         up_ms = path.upload_ms()
-        for _ in range(2):
-            path.step_e2e()
+        n_e2e = max(1, min(args.steps, 10))
+        path.upload(0)
+        for k in range(4):                       # warm-up: the same pipeline
+            path.step_e2e(k)
         torch.cuda.synchronize()
         barrier()
         e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # timed: step 0's upload (nothing to hide it behind), then n steps, each uploading the
+        # next step's inputs while it computes (the last one has no next step)
         e_s.record()
         path.copy_stream.wait_event(e_s)
-        n_e2e = max(1, min(args.steps, 5))
-        for _ in range(n_e2e):
-            path.step_e2e()
+        path.upload(0)
+        for k in range(n_e2e):
+            path.step_e2e(k, upload_next=k + 1 < n_e2e)
         e_e.record()
         torch.cuda.synchronize()
         barrier()
         ems = max_over_ranks(e_s.elapsed_time(e_e))
+        path.use_set(0)
+        # the host link is shared with the machine's other GPUs: its rate just before and just
+        # after the timed steps tells whether a slow end-to-end step was the link's
+        up_after = path.upload_ms()
         e2e = {"value": step_flops(w) * n_e2e * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "ms_per_step": ems / n_e2e, "upload_ms_per_step": up_ms,
-               "h2d_gbs": bi / (up_ms / 1e3) / 1e9}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n_e2e,
+               "ms_per_step": ems / n_e2e, "upload_ms_per_step": [up_ms, up_after],
+               "h2d_gbs": [bi / (up_ms / 1e3) / 1e9, bi / (up_after / 1e3) / 1e9]}
 
     decode = None
     if not args.no_decode:
