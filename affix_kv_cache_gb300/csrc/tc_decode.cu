@@ -24,8 +24,10 @@
 // Warp roles (384 threads, 1 CTA per SM):
 //   warps 0-3   softmax + epilogue: thread r owns TMEM lane r
 //   warp 4      TMEM allocation; lane 0 issues every MMA
-//   warps 8-11  TMA producers: warps 8-9 gather K tiles, 10-11 V tiles (one `tile::gather4`
-//               of 4 pool rows x 64 columns per lane per tile); warp 8 lane 0 loads Q
+//   warps 6-11  TMA producers: warps 6-8 gather K tiles, 9-11 V tiles (a tile's 64
+//               `tile::gather4` loads of 4 pool rows x 64 columns, 21-22 per warp: a gather4
+//               costs its warp tens of cycles of issue, so more warps gather faster); warp 6
+//               lane 0 loads Q
 // TMEM (512 columns): S0 [0,128)  S1 [128,256)  O [256,384)  P0 [384,448)  P1 [448,512).
 //
 // Every mbarrier wait is bounded; a wait that gives up raises a CTA-wide abort flag and
@@ -50,8 +52,10 @@ constexpr int kBM = 128;                  // TMEM lanes / rows of the Q tile
 constexpr int kBN = 128;                  // keys per tile
 constexpr int kStages = 3;                // K ring and V ring depth
 constexpr int kMmaWarp = 4;
-constexpr int kProdWarp = 8;
+constexpr int kProdWarp = 6;              // first TMA producer warp
+constexpr int kPerRing = 3;               // producer warps per ring: K warps 6-8, V 9-11
 constexpr int kThreads = 12 * 32;
+static_assert(kThreads == (kProdWarp + 2 * kPerRing) * 32, "warp roles");
 constexpr int kMaxCluster = 4;
 // Registers: 384 threads x 168 at launch = 64512; the softmax warpgroup grows to 232, the
 // other two shrink to 136: 128*232 + 256*136 = 64512.
@@ -172,112 +176,118 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
     const uint32_t tmem = ctl.tmem_base;
     bool ok = true;
 
-    if (wg == 2) {
-        // ------------------------------------------------------------------ TMA producers
+    if (wg >= 1) {
         setmaxnreg_dec<kRegOther>();
-        const int pw = warp - kProdWarp;
-        if (pw == 0 && lane == 0) {
-            tma_prefetch_desc(&p.tm_q);
-            tma_prefetch_desc(&p.tm_k);
-            tma_prefetch_desc(&p.tm_v);
-            // replica w of the row block lands at lanes [w*G, w*G + qpb*g)
-            mbar_arrive_expect_tx(&ctl.q_full, (uint32_t)(REP * 2 * 128 * p.g * p.qpb));
-            for (int w = 0; w < REP; ++w) {
-                tma_load_4d(sQ + (uint32_t)(w * G) * 128u, &p.tm_q, 0, hk * p.g, q0, b, &ctl.q_full);
-                tma_load_4d(sQ + kRegion + (uint32_t)(w * G) * 128u, &p.tm_q, 64, hk * p.g, q0, b, &ctl.q_full);
-            }
-        }
-        const bool is_v = pw >= 2;
-        uint64_t* full = is_v ? ctl.v_full : ctl.k_full;
-        uint64_t* empty = is_v ? ctl.v_empty : ctl.k_empty;
-        const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
-        const bool leader = (pw & 1) == 0 && lane == 0;
-        const int oob_row = (int)(p.num_slots * p.Hkv);
-        const int x = (pw & 1) * 32 + lane;
-        const int gi = x >> 1, half = x & 1;
-        const int32_t* rs = p.read_slot + (int64_t)b * p.T_len;
-        auto resolve = [&](int j, int (&rows)[4]) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = (kt0 + j) * kBN + 4 * gi + u;
-                rows[u] = oob_row;
-                if (j < n_kv && t < p.T_len) {
-                    const int64_t slot = rs[t];
-                    if (slot >= 0 && slot < p.num_slots)
-                        rows[u] = (int)(slot * p.Hkv + hk);
-                    else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
-                        flag(dev_status, ACACHE_DEV_BAD_SLOT);
+        if (warp >= kProdWarp) {
+            // -------------------------------------------------------------- TMA producers
+            const int pw = warp - kProdWarp;
+            if (pw == 0 && lane == 0) {
+                tma_prefetch_desc(&p.tm_q);
+                tma_prefetch_desc(&p.tm_k);
+                tma_prefetch_desc(&p.tm_v);
+                // replica w of the row block lands at lanes [w*G, w*G + qpb*g)
+                mbar_arrive_expect_tx(&ctl.q_full, (uint32_t)(REP * 2 * 128 * p.g * p.qpb));
+                for (int w = 0; w < REP; ++w) {
+                    tma_load_4d(sQ + (uint32_t)(w * G) * 128u, &p.tm_q, 0, hk * p.g, q0, b, &ctl.q_full);
+                    tma_load_4d(sQ + kRegion + (uint32_t)(w * G) * 128u, &p.tm_q, 64, hk * p.g, q0, b, &ctl.q_full);
                 }
             }
-        };
-        int next[4];
-        resolve(0, next);
-        // store-then-attend: wait for the preceding store grid before reading the pool
-        grid_dependency_wait();
-        for (int j = 0; j < n_kv; ++j) {
-            const int s = j % kStages;
-            int rows[4] = {next[0], next[1], next[2], next[3]};
-            resolve(j + 1, next);
-            if (j >= kStages &&
-                !__all_sync(0xffffffffu, wait_bar(&empty[s], ((j / kStages) - 1) & 1, abort_flag, dev_status)))
-                break;
-            if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
-            __syncwarp();
-            tma_gather4((is_v ? sV(s) : sK(s)) + (uint32_t)half * kRegion + (uint32_t)gi * 512u, tm, half * 64,
-                        rows[0], rows[1], rows[2], rows[3], &full[s]);
-        }
-    } else if (wg == 1) {
-        setmaxnreg_dec<kRegOther>();
-        // ------------------------------------------------------------------ MMA issuer
-        // Order: S(0), S(1), then per tile j: PV(j) once P(j) is in TMEM, then S(j+2) into
-        // the buffer P(j)'s scores came from.  MMAs of one thread run in issue order, so the
-        // completion of S(j+2) implies that of PV(j): the softmax of tile j+2 may then
-        // overwrite P buffer j % 2.
-        if (warp == kMmaWarp && lane == 0) {
-            const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-            const uint32_t idO = idesc_bf16(kBM, kD, false, true);
-            const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
-            auto issue_s = [&](int j) {
-                const uint64_t dk = sdesc_sw128(sK(j % kStages), 16, 1024);
-                const uint32_t d_s = tmem + kColS0 + (uint32_t)(j & 1) * 128u;
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint64_t ko = ((uint64_t)(k >> 2) * kRegion + (uint64_t)(k & 3) * 32u) >> 4;
-                    umma_ss(d_s, dq + ko, dk + ko, idS, k > 0);
+            const bool is_v = pw >= kPerRing;
+            const int pi = pw - (is_v ? kPerRing : 0);    // place among the ring's warps
+            uint64_t* full = is_v ? ctl.v_full : ctl.k_full;
+            uint64_t* empty = is_v ? ctl.v_empty : ctl.k_empty;
+            const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
+            const bool leader = pi == 0 && lane == 0;
+            const int oob_row = (int)(p.num_slots * p.Hkv);
+            // this lane's gather x = 4-row group x / 2 of the tile, column half x % 2; lanes with
+            // x >= 64 have none (every warp of the ring still has some in every tile)
+            const int x = kPerRing * lane + pi;
+            const bool gathers = x < 64;
+            const int gi = x >> 1, half = x & 1;
+            const int32_t* rs = p.read_slot + (int64_t)b * p.T_len;
+            auto resolve = [&](int j, int (&rows)[4]) {
+    #pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int t = (kt0 + j) * kBN + 4 * gi + u;
+                    rows[u] = oob_row;
+                    if (gathers && j < n_kv && t < p.T_len) {
+                        const int64_t slot = rs[t];
+                        if (slot >= 0 && slot < p.num_slots)
+                            rows[u] = (int)(slot * p.Hkv + hk);
+                        else if (!is_v && half == 0 && !(kDrop && slot == ACACHE_SLOT_NONE))
+                            flag(dev_status, ACACHE_DEV_BAD_SLOT);
+                    }
                 }
-                umma_commit(&ctl.s_full[j & 1]);
-                umma_commit(&ctl.k_empty[j % kStages]);
             };
-            ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
-            for (int j = 0; ok && j < 2 && j < n_kv; ++j) {
-                ok = wait_bar(&ctl.k_full[j], 0, abort_flag, dev_status);
-                if (!ok) break;
-                tc_fence_after();
-                issue_s(j);
+            int next[4];
+            resolve(0, next);
+            // store-then-attend: wait for the preceding store grid before reading the pool
+            grid_dependency_wait();
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % kStages;
+                int rows[4] = {next[0], next[1], next[2], next[3]};
+                resolve(j + 1, next);
+                if (j >= kStages &&
+                    !__all_sync(0xffffffffu, wait_bar(&empty[s], ((j / kStages) - 1) & 1, abort_flag, dev_status)))
+                    break;
+                if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
+                __syncwarp();
+                if (gathers)
+                    tma_gather4((is_v ? sV(s) : sK(s)) + (uint32_t)half * kRegion + (uint32_t)gi * 512u, tm,
+                                half * 64, rows[0], rows[1], rows[2], rows[3], &full[s]);
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                ok = wait_bar(&ctl.v_full[j % kStages], (j / kStages) & 1, abort_flag, dev_status) &&
-                     wait_bar(&ctl.p_full[j & 1], (j >> 1) & 1, abort_flag, dev_status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t dv = sdesc_sw128(sV(j % kStages), kRegion, 1024);
-                const uint32_t a_p = tmem + kColP0 + (uint32_t)(j & 1) * 64u;
-#pragma unroll
-                for (int k = 0; k < kBN / 16; ++k)
-                    umma_ts(tmem + kColO, a_p + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (j > 0 || k > 0));
-                umma_commit(&ctl.v_empty[j % kStages]);
-                umma_commit(&ctl.pv_done);
-                if (j + 2 < n_kv) {
-                    ok = wait_bar(&ctl.k_full[(j + 2) % kStages], ((j + 2) / kStages) & 1, abort_flag, dev_status);
+        } else {
+            // ------------------------------------------------------------------ MMA issuer
+            // Order: S(0), S(1), then per tile j: PV(j) once P(j) is in TMEM, then S(j+2) into
+            // the buffer P(j)'s scores came from.  MMAs of one thread run in issue order, so the
+            // completion of S(j+2) implies that of PV(j): the softmax of tile j+2 may then
+            // overwrite P buffer j % 2.
+            if (warp == kMmaWarp && lane == 0) {
+                const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+                const uint32_t idO = idesc_bf16(kBM, kD, false, true);
+                const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+                auto issue_s = [&](int j) {
+                    const uint64_t dk = sdesc_sw128(sK(j % kStages), 16, 1024);
+                    const uint32_t d_s = tmem + kColS0 + (uint32_t)(j & 1) * 128u;
+    #pragma unroll
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const uint64_t ko = ((uint64_t)(k >> 2) * kRegion + (uint64_t)(k & 3) * 32u) >> 4;
+                        umma_ss(d_s, dq + ko, dk + ko, idS, k > 0);
+                    }
+                    umma_commit(&ctl.s_full[j & 1]);
+                    umma_commit(&ctl.k_empty[j % kStages]);
+                };
+                ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
+                for (int j = 0; ok && j < 2 && j < n_kv; ++j) {
+                    ok = wait_bar(&ctl.k_full[j], 0, abort_flag, dev_status);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(j + 2);
+                    issue_s(j);
                 }
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    ok = wait_bar(&ctl.v_full[j % kStages], (j / kStages) & 1, abort_flag, dev_status) &&
+                         wait_bar(&ctl.p_full[j & 1], (j >> 1) & 1, abort_flag, dev_status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dv = sdesc_sw128(sV(j % kStages), kRegion, 1024);
+                    const uint32_t a_p = tmem + kColP0 + (uint32_t)(j & 1) * 64u;
+    #pragma unroll
+                    for (int k = 0; k < kBN / 16; ++k)
+                        umma_ts(tmem + kColO, a_p + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (j > 0 || k > 0));
+                    umma_commit(&ctl.v_empty[j % kStages]);
+                    umma_commit(&ctl.pv_done);
+                    if (j + 2 < n_kv) {
+                        ok = wait_bar(&ctl.k_full[(j + 2) % kStages], ((j + 2) / kStages) & 1, abort_flag, dev_status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(j + 2);
+                    }
+                }
+                umma_commit(&ctl.drain);
+                mbar_wait(&ctl.drain, 0, kBudget);
             }
-            umma_commit(&ctl.drain);
-            mbar_wait(&ctl.drain, 0, kBudget);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         setmaxnreg_inc<kRegSoftmax>();
         // ------------------------------------------------------------------ softmax
