@@ -17,6 +17,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -278,7 +279,7 @@ class Path:
 
     def upload_ms(self, reps=3):
         """Milliseconds to upload one step's inputs with nothing else running: the host link's
-        share of the end-to-end step (the link is shared with the box's other GPUs)."""
+        share of the end-to-end step (the link is shared with the machine's other GPUs)."""
         torch.cuda.synchronize()
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(self.copy_stream)
@@ -696,8 +697,7 @@ def main():
         return reduce_max(x, dev)
 
     ev = {"select": []}
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/acache_clocks_{rank}.csv")
+    clocks = ClockSampler(os.path.join(tempfile.gettempdir(), f"acache_clocks_{os.getpid()}_r{rank}.csv"))
     barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests never run on a host without a GPU; they are selected with -m gpu on a GPU machine.
+    # GPU tests never run on a host without a GPU; they are selected with -m gpu on a host with a GPU.
     try:
         import torch
         has_gpu = torch.cuda.is_available()
