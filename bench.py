@@ -79,11 +79,11 @@ def measured_peaks():
             "source": "fallback"}
 
 
-def profiled_traffic(kernel_files):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
-    if the summary is missing or the kernel source changed since it was captured."""
+def profiled_traffic(kernel_files, summary="slot_attention_llada8b_prefix.md"):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, or None if the
+    summary is missing or the kernel source changed since it was captured."""
     import hashlib
-    summ = os.path.join(ROOT, "profiles", "slot_attention_llada8b_prefix.md")
+    summ = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(summ):
         return None
     fields = {}
@@ -380,7 +380,9 @@ class Decode:
             "roofline": {"bound": "hbm", "kernel": "decode_slot_attention", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "peak_source": f"{peaks['source']} HBM copy",
-                         "bytes_per_launch": self.unique_bytes, "traffic": None},
+                         "bytes_per_launch": self.unique_bytes,
+                         "traffic": profiled_traffic(["affix_kv_cache_gb300/csrc/tc_decode.cu"],
+                                                     "decode_slot_attention_llada8b_prefix.md")},
         }
 
 
