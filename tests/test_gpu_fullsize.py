@@ -176,3 +176,46 @@ def test_fullsize_gather_matches_store():
     ac.acache_gather_slots(desc_of(w), w.batch, w.T, rsd, kc, vc, lay.num_slots, ko, vo)
     torch.cuda.synchronize()
     assert torch.equal(ko, kc[rsd.long()]) and torch.equal(vo, vc[rsd.long()])
+
+
+def test_fullsize_chained_layers_repeat():
+    """One recompute point over 8 layers of the LLaDA-8B prefix workload in one call (chained
+    grids, each released once its predecessor's CTAs have all started), repeated: every run
+    ends with no device error and matches the per-layer calls bit for bit.  Its lone query
+    tiles split their keys, and the second half of those keys is box-loaded (the request's
+    own rows sit in consecutive slots) -- the case whose producer warps once fell two barrier
+    phases behind and stalled the CTA."""
+    w = wl.LLADA_PREFIX
+    layers, reps = 8, 6
+    lay = wl.slot_layout(w)
+    anchors = seeded_anchors(w)
+    d = desc_of(w)
+    st = status_tensor()
+    _, rs = oracle.build_slot_maps(anchors, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+    rsd = torch.from_numpy(rs).cuda()
+    wslot = lay.private_slots.cuda()
+    kc, vc, kn, vn, q = [], [], [], [], []
+    for n in range(layers):
+        inp = wl.probe_inputs(w, n, device="cuda")
+        rec = wl.recompute_inputs(w, n, 0, device="cuda")
+        k = torch.zeros((lay.num_slots, w.hkv, w.d), dtype=torch.bfloat16, device="cuda")
+        v = torch.zeros_like(k)
+        ac.acache_write_slots(d, 1, w.L, lay.shared_slot.cuda(), inp["k_aff"], inp["v_aff"], k, v,
+                              lay.num_slots, 0, dev_status=st)
+        kc.append(k), vc.append(v), kn.append(rec["k_new"]), vn.append(rec["v_new"]), q.append(rec["q_r"])
+    ref = [torch.empty_like(x) for x in q]
+    for n in range(layers):
+        ac.acache_store_attend(d, w.batch, w.R, wslot, kn[n], vn[n], kc[n], vc[n], lay.num_slots,
+                               lay.private_begin, w.R, q[n], w.T, rsd, ref[n], dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    out = [torch.empty_like(x) for x in q]
+    for r in range(reps):
+        for o in out:
+            o.zero_()
+        ac.acache_store_attend_layers(d, w.batch, w.R, wslot, kn, vn, kc, vc, lay.num_slots, lay.private_begin,
+                                      w.R, q, w.T, rsd, out, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0, f"device status {st.item()} in run {r}"
+        for n in range(layers):
+            assert torch.equal(out[n], ref[n]), f"run {r}, layer {n}"
