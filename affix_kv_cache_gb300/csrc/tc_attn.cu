@@ -45,12 +45,18 @@
 //   `tile::gather4`; thread r owns affix key r and sums 2^(logit - m_k) / l_k over the masked
 //   rows k into four partial sums in a fixed order -- a per-thread sum, so the result is
 //   deterministic and no cross-thread reduction is needed.
+// tc_colsum_rows_kernel  (the same pass when the masked rows fit in two 128-row chunks; one
+//                         CTA per (request, query head, run of affix tiles))
+//   the masked rows stay in shared memory while the run's affix key tiles stream through
+//   two stages and D alternates between two TMEM buffers; same sums in the same order.
 //
 // Every mbarrier wait is bounded (about a second); a wait that gives up raises a CTA-wide
 // abort flag and ACACHE_DEV_TIMEOUT, every role leaves its loop, in-flight MMAs are drained
 // with a bounded wait, and TMEM is freed before the CTA exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "tc_attn.cuh"
 #include "ptx.cuh"
@@ -933,6 +939,210 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
 }
 
+// ------------------------------------------------------------------------------------------
+// Second probe pass with the masked rows resident (m <= 256: one or two chunks of 128 rows, the
+// usual case).  One CTA per (request, query head, run of affix tiles): the producer loads the
+// masked query rows once, with their statistics, then streams the run's affix key tiles through
+// two stages; the MMA warp computes D_i = K_affix_tile_i Q_masked^T into one of two TMEM
+// buffers (a 128-column block per chunk) while the consumers exponentiate the other.  Thread r
+// of the consumers owns affix key r of every tile and sums exactly as tc_colsum_kernel does
+// (chunk by chunk, masked row k into partial sum k % 4), so both kernels give the same bits.
+constexpr int kCrMaxChunks = 2;
+constexpr int kCrMmaWarp = 4;
+constexpr int kCrProdWarp = 5;
+constexpr int kCrThreads = (kCrProdWarp + 1) * 32;
+constexpr uint32_t kCrSmemBytes = kTileBytes * (kCrMaxChunks + 2) + 1024;   // chunks + 2 K stages
+constexpr uint32_t kCrTmemCols = 512;                                      // 2 buffers x 2 chunks
+
+struct ColsumRowsCtl {
+    uint64_t q_full;                  // the masked rows and their statistics
+    uint64_t k_full[2], k_empty[2];   // affix key tile stages
+    uint64_t d_full[2];               // D buffer i holds the scores of a tile
+    uint64_t cons_done[2];            // the consumers are done with D buffer i
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    float st_m[kCrMaxChunks][kBN];    // row maximum (log2 domain) of each masked row; +inf = skip
+    float st_il[kCrMaxChunks][kBN];   // 1 / row sum; 0 = skip
+};
+
+__global__ void __launch_bounds__(kCrThreads, 1)
+tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta) {
+    extern __shared__ uint8_t dsm[];
+    __shared__ ColsumRowsCtl ctl;
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    auto sQc = [&](int c) { return base + kTileBytes * (uint32_t)c; };
+    auto sKs = [&](int s) { return base + kTileBytes * (uint32_t)(kCrMaxChunks + s); };
+    const int n_jt = (p.L + kBN - 1) / kBN;
+    const int n_grp = (n_jt + tiles_per_cta - 1) / tiles_per_cta;
+    const int grp = blockIdx.x % n_grp;
+    const int h = (blockIdx.x / n_grp) % p.Hq;
+    const int b = blockIdx.x / (n_grp * p.Hq);
+    const int hk = h / (p.Hq / p.Hkv);
+    const int jt0 = grp * tiles_per_cta;
+    const int n_t = min(n_jt, jt0 + tiles_per_cta) - jt0;
+    const int n_ch = (p.m + kBN - 1) / kBN;
+    if (n_t <= 0 || n_ch > kCrMaxChunks) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* abort_flag = &ctl.abort;
+    int32_t* dev_status = p.dev_status;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ctl.q_full, 32);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&ctl.k_full[s], 1);
+            mbar_init(&ctl.k_empty[s], 1);
+            mbar_init(&ctl.d_full[s], 1);
+            mbar_init(&ctl.cons_done[s], 128);
+        }
+        mbar_init(&ctl.drain, 1);
+        ctl.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kCrMmaWarp) {
+        tmem_alloc(&ctl.tmem_base, kCrTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    if (warp == kCrProdWarp) {
+        const float* sm_row = p.stat_m + ((int64_t)b * p.Hq + h) * p.P;
+        const float* sl_row = p.stat_l + ((int64_t)b * p.Hq + h) * p.P;
+        const int32_t* mrow = p.masked + (int64_t)b * p.m;
+        const int oob_row = p.B * p.P * p.Hq;               // first row outside the queries
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_kaff);
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_qbox);
+        }
+        // The masked rows: every lane stores its rows' statistics, then arrives on q_full (lane
+        // 0 through the expect_tx that announces all chunks' bytes, before any load is issued).
+        int rows[kCrMaxChunks][4], r0[kCrMaxChunks];
+        bool run[kCrMaxChunks];
+#pragma unroll
+        for (int c = 0; c < kCrMaxChunks; ++c) {
+            run[c] = false;
+            r0[c] = 0;
+            if (c >= n_ch) continue;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = c * kBN + 4 * lane + u;
+                const int pr = k < p.m ? mrow[k] : -1;
+                const bool good = pr >= 0 && pr < p.P;
+                if (k < p.m && !good) flag(dev_status, ACACHE_DEV_BAD_ROW);
+                rows[c][u] = good ? ((b * p.P + pr) * p.Hq + h) : oob_row;
+                ctl.st_m[c][4 * lane + u] = good ? sm_row[pr] : INFINITY;
+                ctl.st_il[c][4 * lane + u] = good ? 1.f / sl_row[pr] : 0.f;
+            }
+            // a chunk of consecutive probe rows (the generation positions) is two tiled box
+            // loads; rows of the box past the masked set are skipped by their statistics
+            r0[c] = __shfl_sync(0xffffffffu, mrow[min(c * kBN, p.m - 1)], 0);
+            bool ok_run = r0[c] >= 0 && r0[c] + kBN <= p.P + kBN;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = c * kBN + 4 * lane + u;
+                if (k < p.m) ok_run = ok_run && mrow[k] == r0[c] + 4 * lane + u;
+            }
+            run[c] = __all_sync(0xffffffffu, ok_run);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&ctl.q_full, kTileBytes * (uint32_t)n_ch);
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < kCrMaxChunks; ++c) {
+            if (c >= n_ch) continue;
+            if (run[c]) {
+                if (lane == 0) {
+                    tma_load_4d(sQc(c), &p.tm_qbox, 0, h, r0[c], b, &ctl.q_full);
+                    tma_load_4d(sQc(c) + kRegion, &p.tm_qbox, 64, h, r0[c], b, &ctl.q_full);
+                }
+            } else {
+                const uint32_t o = (uint32_t)lane * 512u;
+                tma_gather4(sQc(c) + o, &p.tm_q, 0, rows[c][0], rows[c][1], rows[c][2], rows[c][3], &ctl.q_full);
+                tma_gather4(sQc(c) + kRegion + o, &p.tm_q, 64, rows[c][0], rows[c][1], rows[c][2], rows[c][3],
+                            &ctl.q_full);
+            }
+        }
+        if (lane != 0) mbar_arrive(&ctl.q_full);
+        // the run's affix key tiles, two stages
+        for (int i = 0; i < n_t; ++i) {
+            const int s = i & 1;
+            if (i >= 2 &&
+                !__all_sync(0xffffffffu, wait_bar(&ctl.k_empty[s], ((i >> 1) - 1) & 1, abort_flag, dev_status)))
+                break;
+            if (lane == 0) {
+                const int j0 = (jt0 + i) * kBN;
+                mbar_arrive_expect_tx(&ctl.k_full[s], kTileBytes);
+                tma_load_3d(sKs(s), &p.tm_kaff, 0, hk, j0, &ctl.k_full[s]);
+                tma_load_3d(sKs(s) + kRegion, &p.tm_kaff, 64, hk, j0, &ctl.k_full[s]);
+            }
+            __syncwarp();
+        }
+    } else if (warp == kCrMmaWarp) {
+        if (lane == 0) {
+            const uint32_t id = idesc_bf16(kBN, kBN, false, false);
+            bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
+            for (int i = 0; ok && i < n_t; ++i) {
+                const int s = i & 1;
+                ok = wait_bar(&ctl.k_full[s], (i >> 1) & 1, abort_flag, dev_status);
+                if (ok && i >= 2) ok = wait_bar(&ctl.cons_done[s], ((i >> 1) - 1) & 1, abort_flag, dev_status);
+                if (!ok) break;
+                tc_fence_after();
+                for (int c = 0; c < n_ch; ++c) {
+#pragma unroll
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const uint32_t ko = (uint32_t)(k >> 2) * kRegion + (uint32_t)(k & 3) * 32u;
+                        umma_ss(tmem + (uint32_t)s * 256u + (uint32_t)c * kBN, sdesc_sw128(sKs(s) + ko, 16, 1024),
+                                sdesc_sw128(sQc(c) + ko, 16, 1024), id, k > 0);
+                    }
+                }
+                umma_commit(&ctl.d_full[s]);
+                umma_commit(&ctl.k_empty[s]);
+            }
+            umma_commit(&ctl.drain);
+            mbar_wait(&ctl.drain, 0, kBudget);
+        }
+        __syncwarp();
+    } else {
+        const int r = threadIdx.x;                         // affix key r of every tile
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float c2 = p.scale_log2;
+        bool ok = __all_sync(0xffffffffu, wait_bar(&ctl.q_full, 0, abort_flag, dev_status));
+        for (int i = 0; ok && i < n_t; ++i) {
+            const int s = i & 1;
+            ok = __all_sync(0xffffffffu, wait_bar(&ctl.d_full[s], (i >> 1) & 1, abort_flag, dev_status));
+            if (!ok) break;
+            tc_fence_after();
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < n_ch; ++c) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + (uint32_t)s * 256u + (uint32_t)c * kBN + cc * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int k = cc * 32 + e;
+                        acc4[e & 3] = fmaf(fast_exp2(fmaf(__uint_as_float(v[e]), c2, -ctl.st_m[c][k])),
+                                           ctl.st_il[c][k], acc4[e & 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&ctl.cons_done[s]);
+            const int j = (jt0 + i) * kBN + r;
+            if (j < p.L) p.partial[((int64_t)b * p.Hq + h) * p.L + j] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kCrMmaWarp) tmem_dealloc(tmem, kCrTmemCols);
+}
+
 // pdl: launched with programmatic stream serialisation after a grid that releases it early --
 // a store (store-then-attend; prm.early_wait orders the pool reads after it) or the attention
 // of another layer (chained layers; prm.early_wait = 0).
@@ -1093,6 +1303,23 @@ int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
     prm.scale_log2 = a.scale * kLog2e;
+    if ((m + kBN - 1) / kBN <= kCrMaxChunks) {
+        // masked rows resident: one CTA per (request, head) and run of affix tiles, the runs
+        // as long as the SMs allow (one CTA per SM)
+        const int n_jt = (L + kBN - 1) / kBN;
+        const int64_t bh = (int64_t)B * a.hq;
+        const int64_t fit = std::max<int64_t>(1, (int64_t)sm_count() / bh);
+        const int per = (int)((n_jt + std::min<int64_t>(n_jt, fit) - 1) / std::min<int64_t>(n_jt, fit));
+        const int64_t ctas_r = bh * ((n_jt + per - 1) / per);
+        if (ctas_r > 0x7fffffff) return ACACHE_ERR_INVALID_ARG;
+        if (cudaFuncSetAttribute(tc_colsum_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kCrSmemBytes) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return ACACHE_ERR_CUDA;
+        }
+        tc_colsum_rows_kernel<<<(unsigned)ctas_r, kCrThreads, kCrSmemBytes, stream>>>(prm, per);
+        return launch_status();
+    }
     if (cudaFuncSetAttribute(tc_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kCsSmemBytes) != cudaSuccess) {
         (void)cudaGetLastError();
