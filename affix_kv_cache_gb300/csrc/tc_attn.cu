@@ -48,7 +48,7 @@
 // tc_colsum_rows_kernel  (the same pass when the masked rows fit in two 128-row chunks; one
 //                         CTA per (request, query head, run of affix tiles))
 //   the masked rows stay in shared memory while the run's affix key tiles stream through
-//   two stages and D alternates between two TMEM buffers; same sums in the same order.
+//   four stages and D alternates between two TMEM buffers; one consumer warpgroup per chunk.
 //
 // Every mbarrier wait is bounded (about a second); a wait that gives up raises a CTA-wide
 // abort flag and ACACHE_DEV_TIMEOUT, every role leaves its loop, in-flight MMAs are drained
@@ -943,27 +943,30 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
 // Second probe pass with the masked rows resident (m <= 256: one or two chunks of 128 rows, the
 // usual case).  One CTA per (request, query head, run of affix tiles): the producer loads the
 // masked query rows once, with their statistics, then streams the run's affix key tiles through
-// two stages; the MMA warp computes D_i = K_affix_tile_i Q_masked^T into one of two TMEM
-// buffers (a 128-column block per chunk) while the consumers exponentiate the other.  Thread r
-// of the consumers owns affix key r of every tile and sums exactly as tc_colsum_kernel does
-// (chunk by chunk, masked row k into partial sum k % 4), so both kernels give the same bits.
+// four stages; the MMA warp computes D_i = K_affix_tile_i Q_masked^T into one of two TMEM
+// buffers (a 128-column block per chunk) while the consumers exponentiate the other.  Consumer
+// warpgroup g takes chunk g; its thread r owns affix key r of every tile and sums over the
+// chunk's masked rows k into four partial sums (k % 4), added in a fixed order; the second
+// warpgroup hands its sum to the first through shared memory, which adds it last.
 constexpr int kCrMaxChunks = 2;
-constexpr int kCrMmaWarp = 4;
-constexpr int kCrProdWarp = 5;
+constexpr int kCrMmaWarp = 8;                 // warps 0-7: two consumer warpgroups
+constexpr int kCrProdWarp = 9;
 constexpr int kCrThreads = (kCrProdWarp + 1) * 32;
-constexpr uint32_t kCrSmemBytes = kTileBytes * (kCrMaxChunks + 2) + 1024;   // chunks + 2 K stages
+constexpr int kCrKStages = 4;                 // affix key tile stages
+constexpr uint32_t kCrSmemBytes = kTileBytes * (kCrMaxChunks + kCrKStages) + 1024;
 constexpr uint32_t kCrTmemCols = 512;                                      // 2 buffers x 2 chunks
 
 struct ColsumRowsCtl {
     uint64_t q_full;                  // the masked rows and their statistics
-    uint64_t k_full[2], k_empty[2];   // affix key tile stages
+    uint64_t k_full[kCrKStages], k_empty[kCrKStages];   // affix key tile stages
     uint64_t d_full[2];               // D buffer i holds the scores of a tile
     uint64_t cons_done[2];            // the consumers are done with D buffer i
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    float st_m[kCrMaxChunks][kBN];    // row maximum (log2 domain) of each masked row; +inf = skip
-    float st_il[kCrMaxChunks][kBN];   // 1 / row sum; 0 = skip
+    float st_off[kCrMaxChunks][kBN];  // per masked row: row maximum (log2 domain) + log2(row
+                                      // sum), so its probabilities are 2^(logit - off); +inf = skip
+    float xsum[2][kBN];               // the second consumer warpgroup's sums, by tile parity
 };
 
 __global__ void __launch_bounds__(kCrThreads, 1)
@@ -989,11 +992,13 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 32);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kCrKStages; ++s) {
             mbar_init(&ctl.k_full[s], 1);
             mbar_init(&ctl.k_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&ctl.d_full[s], 1);
-            mbar_init(&ctl.cons_done[s], 128);
+            mbar_init(&ctl.cons_done[s], 256);
         }
         mbar_init(&ctl.drain, 1);
         ctl.abort = 0;
@@ -1034,8 +1039,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
                 const bool good = pr >= 0 && pr < p.P;
                 if (k < p.m && !good) flag(dev_status, ACACHE_DEV_BAD_ROW);
                 rows[c][u] = good ? ((b * p.P + pr) * p.Hq + h) : oob_row;
-                ctl.st_m[c][4 * lane + u] = good ? sm_row[pr] : INFINITY;
-                ctl.st_il[c][4 * lane + u] = good ? 1.f / sl_row[pr] : 0.f;
+                ctl.st_off[c][4 * lane + u] = good ? sm_row[pr] + log2f(sl_row[pr]) : INFINITY;
             }
             // a chunk of consecutive probe rows (the generation positions) is two tiled box
             // loads; rows of the box past the masked set are skipped by their statistics
@@ -1067,11 +1071,12 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
             }
         }
         if (lane != 0) mbar_arrive(&ctl.q_full);
-        // the run's affix key tiles, two stages
+        // the run's affix key tiles, kCrKStages stages
         for (int i = 0; i < n_t; ++i) {
-            const int s = i & 1;
-            if (i >= 2 &&
-                !__all_sync(0xffffffffu, wait_bar(&ctl.k_empty[s], ((i >> 1) - 1) & 1, abort_flag, dev_status)))
+            const int s = i % kCrKStages;
+            if (i >= kCrKStages &&
+                !__all_sync(0xffffffffu,
+                            wait_bar(&ctl.k_empty[s], ((i / kCrKStages) - 1) & 1, abort_flag, dev_status)))
                 break;
             if (lane == 0) {
                 const int j0 = (jt0 + i) * kBN;
@@ -1086,55 +1091,61 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
             const uint32_t id = idesc_bf16(kBN, kBN, false, false);
             bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
             for (int i = 0; ok && i < n_t; ++i) {
-                const int s = i & 1;
-                ok = wait_bar(&ctl.k_full[s], (i >> 1) & 1, abort_flag, dev_status);
-                if (ok && i >= 2) ok = wait_bar(&ctl.cons_done[s], ((i >> 1) - 1) & 1, abort_flag, dev_status);
+                const int ks = i % kCrKStages, db = i & 1;     // key stage, D buffer
+                ok = wait_bar(&ctl.k_full[ks], (i / kCrKStages) & 1, abort_flag, dev_status);
+                if (ok && i >= 2) ok = wait_bar(&ctl.cons_done[db], ((i >> 1) - 1) & 1, abort_flag, dev_status);
                 if (!ok) break;
                 tc_fence_after();
                 for (int c = 0; c < n_ch; ++c) {
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
                         const uint32_t ko = (uint32_t)(k >> 2) * kRegion + (uint32_t)(k & 3) * 32u;
-                        umma_ss(tmem + (uint32_t)s * 256u + (uint32_t)c * kBN, sdesc_sw128(sKs(s) + ko, 16, 1024),
+                        umma_ss(tmem + (uint32_t)db * 256u + (uint32_t)c * kBN, sdesc_sw128(sKs(ks) + ko, 16, 1024),
                                 sdesc_sw128(sQc(c) + ko, 16, 1024), id, k > 0);
                     }
                 }
-                umma_commit(&ctl.d_full[s]);
-                umma_commit(&ctl.k_empty[s]);
+                umma_commit(&ctl.d_full[db]);
+                umma_commit(&ctl.k_empty[ks]);
             }
             umma_commit(&ctl.drain);
             mbar_wait(&ctl.drain, 0, kBudget);
         }
         __syncwarp();
     } else {
-        const int r = threadIdx.x;                         // affix key r of every tile
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int cg = warp >> 2;                          // consumer warpgroup = its chunk
+        const int r = threadIdx.x & 127;                   // affix key r of every tile
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float c2 = p.scale_log2;
-        bool ok = __all_sync(0xffffffffu, wait_bar(&ctl.q_full, 0, abort_flag, dev_status));
-        for (int i = 0; ok && i < n_t; ++i) {
+        bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
+        for (int i = 0; i < n_t; ++i) {
             const int s = i & 1;
-            ok = __all_sync(0xffffffffu, wait_bar(&ctl.d_full[s], (i >> 1) & 1, abort_flag, dev_status));
+            ok = ok && wait_bar(&ctl.d_full[s], (i >> 1) & 1, abort_flag, dev_status);
+            // both warpgroups take the same decision, so neither waits for the other in vain
+            ok = named_barrier_and<1>(256, ok);
             if (!ok) break;
             tc_fence_after();
             float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int c = 0; c < n_ch; ++c) {
+            if (cg < n_ch) {
+                // the chunk's 128 columns in one round trip to TMEM
+                uint32_t v[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    tmem_ld32(lane_base + (uint32_t)s * 256u + (uint32_t)cg * kBN + cc * 32, v[cc]);
+                tmem_ld_wait();
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(lane_base + (uint32_t)s * 256u + (uint32_t)c * kBN + cc * 32, v);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int k = cc * 32 + e;
-                        acc4[e & 3] = fmaf(fast_exp2(fmaf(__uint_as_float(v[e]), c2, -ctl.st_m[c][k])),
-                                           ctl.st_il[c][k], acc4[e & 3]);
-                    }
+                    for (int e = 0; e < 32; ++e)
+                        acc4[e & 3] += fast_exp2(fmaf(__uint_as_float(v[cc][e]), c2, -ctl.st_off[cg][cc * 32 + e]));
                 }
             }
             tc_fence_before();
             mbar_arrive(&ctl.cons_done[s]);
+            const float sum = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+            if (cg == 1) ctl.xsum[s][r] = sum;
+            named_barrier_sync<2>(256);
             const int j = (jt0 + i) * kBN + r;
-            if (j < p.L) p.partial[((int64_t)b * p.Hq + h) * p.L + j] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+            if (cg == 0 && j < p.L) p.partial[((int64_t)b * p.Hq + h) * p.L + j] = sum + ctl.xsum[s][r];
         }
     }
     tc_fence_before();
