@@ -174,6 +174,28 @@ def test_probe_parity(layout, dtype, d, heads):
     assert_scores_close(scores.cpu().numpy(), ref["scores"], "probe scores")
 
 
+@pytest.mark.parametrize("m,consecutive", [(256, True), (257, True), (400, True), (200, False), (300, False)])
+def test_probe_parity_masked_row_counts(m, consecutive):
+    """Up to 256 masked rows (two 128-row chunks) the masked-to-affix mass keeps them resident
+    in shared memory; more go through the one-tile-per-CTA kernel.  Consecutive masked rows
+    are box loads, scattered ones gathered."""
+    w = tiny([(wl.SEG_AFFIX, 400), (wl.SEG_REQ, 100), (wl.SEG_MASK, 300)], batch=2)
+    if consecutive:
+        rows = list(range(w.P - m, w.P))
+    else:
+        rows = sorted(np.random.default_rng(m).choice(w.P, m, replace=False).tolist())
+    inp = wl.probe_inputs(w, 0)
+    ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
+                             T=w.T, l=w.l, masked_rows=rows, scale=w.scale, want_out=False)
+    scores = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    st = status_tensor()
+    probe_layer_gpu(w, inp, scores, masked=torch.tensor(rows, dtype=torch.int32).expand(w.batch, -1),
+                    out=False, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_scores_close(scores.cpu().numpy(), ref["scores"], f"{m} masked rows")
+
+
 def test_probe_accumulates_over_layers_and_is_deterministic():
     w = tiny(RAGGED["infix"], batch=2).replace(layers=3)
     ref = None
