@@ -731,6 +731,11 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+    // A grid of a chain of layers reads nothing its predecessor writes, so it never waited
+    // for it; it waits before its CTAs exit instead, so the grids of a chain complete in
+    // launch order and work behind the chain on the stream sees every layer's output.  (The
+    // predecessor has long finished by then: this grid started in its last wave.)
+    if (!p.early_wait && threadIdx.x == 0) grid_dependency_wait();
 }
 
 // ------------------------------------------------------------------------------------------
