@@ -238,6 +238,21 @@ ACACHE_DEVFN void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
                  : "memory");
 }
 ACACHE_DEVFN void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Abort path of a TMA-fed kernel.  Loads issued before a bounded wait gave up land within
+// microseconds, but the barrier phase they count toward may never complete, so there is
+// nothing to wait on: the CTA is held for a bounded ~30 us instead, so none of them lands in
+// shared memory after the CTA has exited.  Call after the roles' final __syncthreads with a
+// flag every thread reads alike.
+ACACHE_DEVFN void settle_after_abort(bool aborted) {
+    if (!aborted) return;
+    if (threadIdx.x == 0) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 60000) {
+        }
+    }
+    __syncthreads();
+}
 ACACHE_DEVFN void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---- programmatic dependent launch ---------------------------------------------------------

@@ -52,7 +52,8 @@
 //
 // Every mbarrier wait is bounded (about a second); a wait that gives up raises a CTA-wide
 // abort flag and ACACHE_DEV_TIMEOUT, every role leaves its loop, in-flight MMAs are drained
-// with a bounded wait, and TMEM is freed before the CTA exits.
+// with a bounded wait, TMA loads issued before the abort get a bounded ~30 us to land, and
+// TMEM is freed before the CTA exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -730,6 +731,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    settle_after_abort(*abort_flag != 0);
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
     // A grid of a chain of layers reads nothing its predecessor writes, so it never waited
     // for it; it waits before its CTAs exit instead, so the grids of a chain complete in
@@ -941,6 +943,7 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    settle_after_abort(*abort_flag != 0);
     if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
 }
 
@@ -1156,6 +1159,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    settle_after_abort(*abort_flag != 0);
     if (warp == kCrMmaWarp) tmem_dealloc(tmem, kCrTmemCols);
 }
 

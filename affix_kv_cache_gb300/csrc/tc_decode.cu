@@ -31,8 +31,9 @@
 // TMEM (512 columns): S0 [0,128)  S1 [128,256)  O [256,384)  P0 [384,448)  P1 [448,512).
 //
 // Every mbarrier wait is bounded; a wait that gives up raises a CTA-wide abort flag and
-// ACACHE_DEV_TIMEOUT, roles leave their loops, in-flight MMAs are drained with a bounded wait
-// and TMEM is freed before the CTA exits; the cluster barriers are reached on every path.
+// ACACHE_DEV_TIMEOUT, roles leave their loops, in-flight MMAs are drained with a bounded wait,
+// TMA loads issued before the abort get a bounded ~30 us to land, and TMEM is freed before the
+// CTA exits; the cluster barriers are reached on every path.
 #include <cuda.h>
 
 #include <algorithm>
@@ -457,6 +458,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    settle_after_abort(*abort_flag != 0);
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
     if (REP == 1 && cs == 1) return;
 
