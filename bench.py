@@ -79,9 +79,10 @@ def measured_peaks():
             "source": "fallback"}
 
 
-def profiled_traffic(kernel_files, summary="slot_attention_llada8b_prefix.md"):
+def profiled_traffic(kernel_files, workload, summary="slot_attention_llada8b_prefix.md"):
     """DRAM bytes per launch of a kernel from its committed ncu summary, or None if the
-    summary is missing or the kernel source changed since it was captured."""
+    summary is missing, was taken on another workload, or the kernel source changed since it
+    was captured."""
     import hashlib
     summ = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(summ):
@@ -94,7 +95,7 @@ def profiled_traffic(kernel_files, summary="slot_attention_llada8b_prefix.md"):
     h = hashlib.sha256()
     for f in kernel_files:
         h.update(open(os.path.join(ROOT, f), "rb").read())
-    if fields.get("source_sha256") != h.hexdigest()[:16]:
+    if fields.get("source_sha256") != h.hexdigest()[:16] or fields.get("workload") != workload:
         return None
     try:
         return float(fields["dram_bytes_per_launch"])
@@ -381,7 +382,7 @@ class Decode:
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "peak_source": f"{peaks['source']} HBM copy",
                          "bytes_per_launch": self.unique_bytes,
-                         "traffic": profiled_traffic(["affix_kv_cache_gb300/csrc/tc_decode.cu"],
+                         "traffic": profiled_traffic(["affix_kv_cache_gb300/csrc/tc_decode.cu"], w.name,
                                                      "decode_slot_attention_llada8b_prefix.md")},
         }
 
@@ -719,7 +720,7 @@ def main():
     peaks = measured_peaks()
     slot_achieved = slot_flops_per_launch(w) / (slot_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
-    traffic = profiled_traffic(["affix_kv_cache_gb300/csrc/tc_attn.cu"])
+    traffic = profiled_traffic(["affix_kv_cache_gb300/csrc/tc_attn.cu"], w.name)
 
     e2e = None
     if not args.no_e2e:
