@@ -11,5 +11,5 @@ from ._lib import (AcacheError, AttnDesc, attn_desc, acache_build_slot_maps,  # 
                    acache_probe_workspace_bytes,
                    acache_slot_attention, acache_slot_attention_dropna, acache_slot_attention_varlen,
                    acache_rerotate_keys, acache_store_attend, acache_store_attend_layers, acache_topk_anchors, Pool,
-                   acache_write_slots, lib,
+                   acache_wait_budget, acache_write_slots, lib,
                    status_string, version)

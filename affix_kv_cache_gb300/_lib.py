@@ -28,7 +28,7 @@ SLOT_NONE = -1
 DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
 DEV_BAD_LENGTH = 64
 
-EXPORTS = ("acache_status_string", "acache_version", "acache_probe_workspace_bytes",
+EXPORTS = ("acache_status_string", "acache_version", "acache_wait_budget", "acache_probe_workspace_bytes",
            "acache_probe_scores", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
            "acache_write_slots", "acache_slot_attention", "acache_gather_slots",
            "acache_kv_deviation_scores", "acache_slot_attention_dropna", "acache_slot_attention_varlen",
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         sig = {
             "acache_status_string": (ctypes.c_char_p, [I]),
             "acache_version": (I, []),
+            "acache_wait_budget": (I64, [I64]),
             "acache_probe_workspace_bytes": (S, [D, I, I, I, I]),
             "acache_probe_scores": (I, [D, I, I, I, I, P, I, P, P, P, P, P, P, P, P, S, P, P]),
             "acache_probe_scores_noalloc": (I, [D, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P]),
@@ -133,6 +134,12 @@ def _check(fn, status):
     if status != ACACHE_OK:
         raise AcacheError(fn, status)
     return status
+
+
+def acache_wait_budget(cycles: int = 0) -> int:
+    """Set (cycles > 0) or read (cycles <= 0) the SM-cycle budget of the kernels' bounded
+    waits; returns the budget in force before the call (see include/acache.h)."""
+    return int(lib().acache_wait_budget(int(cycles)))
 
 
 def acache_probe_workspace_bytes(desc, batch, seq_len, affix_len, num_masked) -> int:

@@ -2,6 +2,8 @@
 // dispatch.  Every entry point is declared and documented in include/acache.h.
 #include <math.h>
 
+#include <atomic>
+
 #include "attn.cuh"
 #include "tc_attn.cuh"
 
@@ -24,6 +26,13 @@ int launch_status() {
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ACACHE_OK : ACACHE_ERR_CUDA;
 }
+
+namespace {
+constexpr long long kDefaultWaitBudget = 1LL << 31;   // SM clock cycles: about 1 s at 2.07 GHz
+std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
+}  // namespace
+
+long long wait_budget() { return g_wait_budget.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -118,6 +127,59 @@ int slot_attention(const acache_attn_desc* desc, int batch, int n_q, const void*
 }  // namespace
 }  // namespace acache
 
+namespace acache {
+
+int probe_check(const acache_attn_desc* desc, int batch, int seq_len, int affix_begin, int affix_len,
+                const int32_t* masked_rows, int num_masked, const void* q, const void* k_req,
+                const void* v_req, const void* k_affix, const void* v_affix, void* out, float* scores,
+                ProbeCall* c, bool* empty) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    const int T = seq_len, l = affix_begin, L = affix_len, m = num_masked;
+    if (batch < 0 || T < 0 || l < 0 || L < 0 || (int64_t)l + L > T || m < 0 || m > T - L)
+        return ACACHE_ERR_INVALID_ARG;
+    *empty = batch == 0 || T == L;      // no probe rows: nothing attends
+    if (*empty) return ACACHE_OK;
+    if (!q || !k_req || !v_req || (L > 0 && (!k_affix || !v_affix)) || (m > 0 && !masked_rows) ||
+        (L > 0 && !scores))
+        return ACACHE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_req) || !aligned16(v_req) || !aligned16(k_affix) ||
+        !aligned16(v_affix) || !aligned16(out))
+        return ACACHE_ERR_INVALID_ARG;
+    *c = ProbeCall{a, batch, T, l, L, m, masked_rows, q, k_req, v_req, k_affix, v_affix, out, scores};
+    return ACACHE_OK;
+}
+
+size_t probe_scratch_bytes(const ProbeCall& c) {
+    return carve_probe_ws(nullptr, c.B, c.a.hq, c.T - c.L, c.L).bytes;
+}
+
+int probe_launch(const ProbeCall& c, void* scratch, int32_t* dev_status, cudaStream_t stream) {
+    const AttnArgs& a = c.a;
+    const ProbeWorkspace ws = carve_probe_ws(scratch, c.B, a.hq, c.T - c.L, c.L);
+    int rc;
+    if (tc_supported(a)) {
+        rc = launch_tc_probe_pass_a(a, c.B, c.T, c.l, c.L, c.q, c.k_req, c.v_req, c.k_aff, c.v_aff, c.out,
+                                    ws.stat_m, ws.stat_l, dev_status, stream);
+    } else {
+        rc = launch_simt_probe_pass_a(a, c.B, c.T, c.l, c.L, c.q, c.k_req, c.v_req, c.k_aff, c.v_aff, c.out,
+                                      ws.stat_m, ws.stat_l, stream);
+    }
+    if (rc) return rc;
+    if (c.L == 0) return ACACHE_OK;
+    if (tc_supported(a)) {
+        rc = launch_tc_probe_pass_b(a, c.B, c.T, c.L, c.masked, c.m, c.q, c.k_aff, ws.stat_m, ws.stat_l,
+                                    ws.partial, dev_status, stream);
+    } else {
+        rc = launch_simt_probe_pass_b(a, c.B, c.T, c.L, c.masked, c.m, c.q, c.k_aff, ws.stat_m, ws.stat_l,
+                                      ws.partial, dev_status, stream);
+    }
+    if (rc) return rc;
+    return launch_score_reduce(c.B, a.hq, c.L, ws.partial, c.scores, stream);
+}
+
+}  // namespace acache
+
 using namespace acache;
 
 extern "C" {
@@ -134,7 +196,12 @@ const char* acache_status_string(int status) {
     }
 }
 
-int acache_version(void) { return 100; }   // 0.1.0
+int acache_version(void) { return 200; }   // 0.2.0
+
+int64_t acache_wait_budget(int64_t cycles) {
+    if (cycles > 0) return g_wait_budget.exchange(cycles);
+    return g_wait_budget.load();
+}
 
 size_t acache_probe_workspace_bytes(const acache_attn_desc* a, int batch, int seq_len,
                                     int affix_len, int num_masked) {
@@ -149,41 +216,15 @@ int acache_probe_scores(const acache_attn_desc* desc, int batch, int seq_len, in
                         const void* k_affix, const void* v_affix, void* out, float* scores,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         void* stream_) {
-    AttnArgs a;
-    if (int rc = check_desc(desc, &a)) return rc;
-    const int T = seq_len, l = affix_begin, L = affix_len, m = num_masked;
-    if (batch < 0 || T < 0 || l < 0 || L < 0 || (int64_t)l + L > T || m < 0 || m > T - L)
-        return ACACHE_ERR_INVALID_ARG;
-    const int P = T - L;
-    if (batch == 0 || P == 0) return ACACHE_OK;      // no probe rows: nothing attends
-    if (!q || !k_req || !v_req || (L > 0 && (!k_affix || !v_affix)) || (m > 0 && !masked_rows) ||
-        (L > 0 && !scores))
-        return ACACHE_ERR_INVALID_ARG;
-    const ProbeWorkspace ws = carve_probe_ws(workspace, batch, a.hq, P, L);
-    if (!workspace || workspace_bytes < ws.bytes) return ACACHE_ERR_WORKSPACE;
-    if (!aligned16(q) || !aligned16(k_req) || !aligned16(v_req) || !aligned16(k_affix) ||
-        !aligned16(v_affix) || !aligned16(out) || ((uintptr_t)workspace & 255u))
-        return ACACHE_ERR_INVALID_ARG;
-    cudaStream_t stream = (cudaStream_t)stream_;
-    int rc;
-    if (tc_supported(a)) {
-        rc = launch_tc_probe_pass_a(a, batch, T, l, L, q, k_req, v_req, k_affix, v_affix, out,
-                                    ws.stat_m, ws.stat_l, dev_status, stream);
-    } else {
-        rc = launch_simt_probe_pass_a(a, batch, T, l, L, q, k_req, v_req, k_affix, v_affix, out,
-                                      ws.stat_m, ws.stat_l, stream);
-    }
-    if (rc) return rc;
-    if (L == 0) return ACACHE_OK;
-    if (tc_supported(a)) {
-        rc = launch_tc_probe_pass_b(a, batch, T, L, masked_rows, m, q, k_affix, ws.stat_m,
-                                    ws.stat_l, ws.partial, dev_status, stream);
-    } else {
-        rc = launch_simt_probe_pass_b(a, batch, T, L, masked_rows, m, q, k_affix, ws.stat_m,
-                                      ws.stat_l, ws.partial, dev_status, stream);
-    }
-    if (rc) return rc;
-    return launch_score_reduce(batch, a.hq, L, ws.partial, scores, stream);
+    ProbeCall c;
+    bool empty = false;
+    if (int rc = probe_check(desc, batch, seq_len, affix_begin, affix_len, masked_rows, num_masked, q, k_req,
+                             v_req, k_affix, v_affix, out, scores, &c, &empty))
+        return rc;
+    if (empty) return ACACHE_OK;
+    if (!workspace || workspace_bytes < probe_scratch_bytes(c)) return ACACHE_ERR_WORKSPACE;
+    if ((uintptr_t)workspace & 255u) return ACACHE_ERR_INVALID_ARG;
+    return probe_launch(c, workspace, dev_status, (cudaStream_t)stream_);
 }
 
 int acache_topk_anchors(const float* scores, int batch, int affix_len, int k, int32_t* anchors,

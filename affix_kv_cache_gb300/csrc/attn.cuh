@@ -94,6 +94,29 @@ struct ProbeKeys {
     ACACHE_DEVFN const T* vbase(int src) const { return src ? v_req : v_aff; }
 };
 
+// ---- the probe of one layer, shared by the entry points that differ only in where the
+// scratch lives (a caller's workspace, or the library's fixed array) ------------------------
+struct ProbeCall {
+    AttnArgs a;
+    int B, T, l, L, m;
+    const int32_t* masked;
+    const void *q, *k_req, *v_req, *k_aff, *v_aff;
+    void* out;
+    float* scores;
+};
+// Validates a probe call's arguments (errors as acache_probe_scores); on ACACHE_OK, *empty
+// says there is nothing to launch, else *c holds the call.
+int probe_check(const acache_attn_desc* desc, int batch, int seq_len, int affix_begin, int affix_len,
+                const int32_t* masked_rows, int num_masked, const void* q, const void* k_req,
+                const void* v_req, const void* k_affix, const void* v_affix, void* out, float* scores,
+                ProbeCall* c, bool* empty);
+// Scratch bytes of the call: row maximum and row sum [B][Hq][P] and per-head column sums
+// [B][Hq][L], float32, each part 256-byte aligned.
+size_t probe_scratch_bytes(const ProbeCall& c);
+// Launches the probe forward, the masked-to-affix mass and the head sum into c.scores, with the
+// scratch at `scratch` (256-byte aligned, probe_scratch_bytes(c) bytes).
+int probe_launch(const ProbeCall& c, void* scratch, int32_t* dev_status, cudaStream_t stream);
+
 // ---- launchers (host) ---------------------------------------------------------------
 int launch_simt_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,

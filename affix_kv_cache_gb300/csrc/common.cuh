@@ -79,4 +79,5 @@ constexpr float kLog2e = 1.4426950408889634f;
 namespace acache {
 int sm_count();                   // SMs of the current device (cached per device)
 int launch_status();              // ACACHE_OK or ACACHE_ERR_CUDA after a launch
+long long wait_budget();          // cycles a kernel's pipeline wait may take (acache_wait_budget)
 }  // namespace acache

@@ -16,8 +16,10 @@
 //  - every call shares it and it keeps the previous call's contents; nothing in it has to
 //    start at zero (each call writes every byte it reads), but calls whose kernels overlap
 //    on the GPU (different streams, no ordering between them) race on it;
-//  - the first call on a device looks up the array's device address (once per device, with
-//    that device current); make that first call before any stream capture begins.
+//  - the array's device address is looked up on every call made while the stream is not
+//    capturing (so a device reset, which reloads the library's device code, is followed);
+//    a call made during stream capture uses the address of the device's last earlier call,
+//    so the first call on a device must come before any capture.
 #include <mutex>
 
 #include "attn.cuh"
@@ -33,21 +35,26 @@ constexpr size_t kScratchAlign = 256;
 // device address looked up below, never the name itself.
 __device__ __align__(256) unsigned char g_probe_scratch[kStaticScratchBytes];
 
-size_t round_up(size_t x) { return (x + kScratchAlign - 1) / kScratchAlign * kScratchAlign; }
-
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_probe_scratch on the current device (looked up once per device).
-int scratch_address(void** out) {
+// Device address of g_probe_scratch on the current device.  Outside stream capture it is looked
+// up afresh (after a device reset the array may sit elsewhere); during capture the address the
+// device's last earlier call found is used.
+int scratch_address(cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
     }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ACACHE_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* ptr = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&ptr, g_probe_scratch);
         if (e != cudaSuccess || !ptr) {
@@ -55,6 +62,8 @@ int scratch_address(void** out) {
             return ACACHE_ERR_CUDA;
         }
         g_scratch_addr[dev] = ptr;
+    } else if (!g_scratch_addr[dev]) {
+        return ACACHE_ERR_CUDA;     // never called on this device before the capture began
     }
     *out = g_scratch_addr[dev];
     return ACACHE_OK;
@@ -71,49 +80,16 @@ extern "C" int acache_probe_scores_noalloc(const acache_attn_desc* desc, int bat
                                            const void* q, const void* k_req, const void* v_req,
                                            const void* k_affix, const void* v_affix, void* out,
                                            float* scores, int32_t* dev_status, void* stream_) {
-    if (!desc || desc->num_q_heads <= 0 || desc->num_kv_heads <= 0 ||
-        desc->num_q_heads % desc->num_kv_heads || !(desc->scale == desc->scale) ||
-        isinf(desc->scale))
-        return ACACHE_ERR_INVALID_ARG;
-    if (desc->dtype != ACACHE_F32 && desc->dtype != ACACHE_BF16) return ACACHE_ERR_UNSUPPORTED;
-    if (desc->head_dim != 64 && desc->head_dim != 128) return ACACHE_ERR_UNSUPPORTED;
-    const AttnArgs a{desc->num_q_heads, desc->num_kv_heads, desc->head_dim, desc->dtype, desc->scale};
-    const int T = seq_len, l = affix_begin, L = affix_len, m = num_masked;
-    if (batch < 0 || T < 0 || l < 0 || L < 0 || (int64_t)l + L > T || m < 0 || m > T - L)
-        return ACACHE_ERR_INVALID_ARG;
-    const int P = T - L;
-    if (batch == 0 || P == 0) return ACACHE_OK;
-    if (!q || !k_req || !v_req || (L > 0 && (!k_affix || !v_affix)) || (m > 0 && !masked_rows) ||
-        (L > 0 && !scores))
-        return ACACHE_ERR_INVALID_ARG;
-    auto a16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
-    if (!a16(q) || !a16(k_req) || !a16(v_req) || !a16(k_affix) || !a16(v_affix) || !a16(out))
-        return ACACHE_ERR_INVALID_ARG;
-    // scratch: row max, row sum [B][Hq][P] and column sums [B][Hq][L], 256-byte aligned parts
-    const size_t st = round_up((size_t)batch * a.hq * P * sizeof(float));
-    const size_t pa = round_up((size_t)batch * a.hq * L * sizeof(float));
-    if (2 * st + pa > kStaticScratchBytes) return ACACHE_ERR_WORKSPACE;
-    void* base = nullptr;
-    if (int rc = scratch_address(&base)) return rc;
-    float* stat_m = (float*)base;
-    float* stat_l = (float*)((char*)base + st);
-    float* partial = (float*)((char*)base + 2 * st);
+    ProbeCall c;
+    bool empty = false;
+    if (int rc = probe_check(desc, batch, seq_len, affix_begin, affix_len, masked_rows, num_masked, q, k_req,
+                             v_req, k_affix, v_affix, out, scores, &c, &empty))
+        return rc;
+    if (empty) return ACACHE_OK;
+    static_assert(kStaticScratchBytes % kScratchAlign == 0, "whole aligned parts");
+    if (probe_scratch_bytes(c) > kStaticScratchBytes) return ACACHE_ERR_WORKSPACE;
     cudaStream_t stream = (cudaStream_t)stream_;
-    int rc;
-    if (tc_supported(a))
-        rc = launch_tc_probe_pass_a(a, batch, T, l, L, q, k_req, v_req, k_affix, v_affix, out,
-                                    stat_m, stat_l, dev_status, stream);
-    else
-        rc = launch_simt_probe_pass_a(a, batch, T, l, L, q, k_req, v_req, k_affix, v_affix, out,
-                                      stat_m, stat_l, stream);
-    if (rc) return rc;
-    if (L == 0) return ACACHE_OK;
-    if (tc_supported(a))
-        rc = launch_tc_probe_pass_b(a, batch, T, L, masked_rows, m, q, k_affix, stat_m, stat_l,
-                                    partial, dev_status, stream);
-    else
-        rc = launch_simt_probe_pass_b(a, batch, T, L, masked_rows, m, q, k_affix, stat_m, stat_l,
-                                      partial, dev_status, stream);
-    if (rc) return rc;
-    return launch_score_reduce(batch, a.hq, L, partial, scores, stream);
+    void* base = nullptr;
+    if (int rc = scratch_address(stream, &base)) return rc;
+    return probe_launch(c, base, dev_status, stream);
 }

@@ -239,11 +239,11 @@ ACACHE_DEVFN void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
 }
 ACACHE_DEVFN void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Abort path of a TMA-fed kernel.  Loads issued before a bounded wait gave up land within
-// microseconds, but the barrier phase they count toward may never complete, so there is
-// nothing to wait on: the CTA is held for a bounded ~30 us instead, so none of them lands in
-// shared memory after the CTA has exited.  Call after the roles' final __syncthreads with a
-// flag every thread reads alike.
+// Abort path of a TMA-fed kernel, when the loads issued before a bounded wait gave up cannot
+// be waited for (the barrier phase they count toward may never complete): they land within
+// microseconds, so the CTA is held for a fixed ~30 us, and none of them lands in shared memory
+// after the CTA has exited.  Call after the roles' final __syncthreads with a flag every
+// thread reads alike.
 ACACHE_DEVFN void settle_after_abort(bool aborted) {
     if (!aborted) return;
     if (threadIdx.x == 0) {

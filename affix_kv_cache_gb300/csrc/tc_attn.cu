@@ -50,10 +50,11 @@
 //   the masked rows stay in shared memory while the run's affix key tiles stream through
 //   four stages and D alternates between two TMEM buffers; one consumer warpgroup per chunk.
 //
-// Every mbarrier wait is bounded (about a second); a wait that gives up raises a CTA-wide
-// abort flag and ACACHE_DEV_TIMEOUT, every role leaves its loop, in-flight MMAs are drained
-// with a bounded wait, TMA loads issued before the abort get a bounded ~30 us to land, and
-// TMEM is freed before the CTA exits.
+// Every mbarrier wait is bounded (by default about a second; acache_wait_budget sets it); a
+// wait that gives up raises a CTA-wide abort flag and ACACHE_DEV_TIMEOUT, every role leaves its
+// loop, in-flight MMAs are drained with a bounded wait, the attention kernel's TMA loads issued
+// before the abort are waited for (bounded; a fixed ~30 us hold where their barrier phase cannot
+// complete, and in the other kernels), and TMEM is freed before the CTA exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -92,7 +93,10 @@ constexpr uint32_t kTmemCols = 512;               // S_A, S_B, O_A, O_B: 128 fp3
 __host__ __device__ constexpr uint32_t col_s(int t) { return (uint32_t)t * 128u; }
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + (uint32_t)t * 128u; }
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: P values stay below 2^8
-constexpr long long kBudget = 1LL << 31;          // cycles (~1 s) before a wait gives up
+// Waits of the abort path itself (in-flight MMAs, TMA loads already issued) use fixed budgets,
+// whatever budget the pipeline's waits were launched with.
+constexpr long long kDrainBudget = 1LL << 31;     // cycles (~1 s): MMAs issued before an abort
+constexpr long long kLandBudget = 1LL << 21;      // cycles (~1 ms): TMA loads issued before it
 
 enum KeyMode { kSlotKeys = 0, kProbeKeys = 1 };
 
@@ -114,6 +118,7 @@ struct AttnParams {
     int early_wait;       // 1: the pool may have been written by the grid this one follows
     int n_rows, Hq, Hkv, T_len, L, P;
     float scale_log2;
+    long long budget;     // cycles a pipeline wait may take before it gives up
 };
 
 struct AttnCtl {
@@ -129,6 +134,7 @@ struct AttnCtl {
     uint64_t turn[kQT];     // softmax ping-pong: turn[t] completes when tile t may exponentiate
     uint32_t tmem_base;
     int abort;
+    int unlanded;           // abort path: some TMA load issued before the abort may not have landed
     int split_ok;           // split keys: chain B's partial state below is complete
     float split_m[kBM];     //   chain B's row maximum (the exponent offset it used) and row sum
     float split_l[kBM];
@@ -157,15 +163,16 @@ struct KeySchedule {
     }
 };
 
-// Bounded wait that also leaves early once another role has aborted.
+// Bounded wait that also leaves early once another role has aborted: after `budget` cycles it
+// raises the CTA's abort flag and ACACHE_DEV_TIMEOUT.
 ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                           int32_t* dev_status) {
+                           int32_t* dev_status, long long budget) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kBudget) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             flag(dev_status, ACACHE_DEV_TIMEOUT);
             return false;
@@ -257,6 +264,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
+    const long long budget = p.budget;
     // The first key tile's read-slot entries are read by the producer lanes before the set-up
     // below, which hides their latency (warp 12 flags bad slots; see the producers).  The maps
     // are not written by a store grid this launch may overlap.
@@ -289,6 +297,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             mbar_init(&ctl.turn[t], 128);
         }
         ctl.abort = 0;
+        ctl.unlanded = 0;
         ctl.split_ok = 1;
         fence_mbar_init();
         // the Q tiles, as soon as their barrier exists
@@ -378,6 +387,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 // without waiting (that store is complete once this wait returns).
                 if (p.early_wait) grid_dependency_wait();
                 grid_launch_dependents();
+                int armed = -1;                           // last entry this warp arrived on
                 for (int e = 0; e < n_kv; ++e) {          // ring entries in load order
                     const int s = e % nst;
                     const int j = ks.entry_tile(e);           // the key tile entry e holds
@@ -387,8 +397,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     const bool box = next_box;
                     next_box = resolve(e + 1 < n_kv ? ks.entry_tile(e + 1) : n_kv, next, next_slot0);
                     if (e >= nst &&
-                        !__all_sync(0xffffffffu, wait_bar(&empty[s], ((e / nst) - 1) & 1, abort_flag,
-                                                          dev_status)))
+                        !__all_sync(0xffffffffu, wait_bar(&empty[s], ((e / nst) - 1) & 1, abort_flag, dev_status, budget)))
                         break;
                     // The ring's first warp announces the tile's bytes; a gather of another warp
                     // that completes first leaves the count transiently negative (allowed).  Read-
@@ -400,6 +409,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     // twice before a warp busy with the other chain's gathers looked at its stage.)
                     if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
                     else if (kMode == kSlotKeys && lane == 0) mbar_arrive(&full[s]);
+                    armed = e;
                     __syncwarp();
                     if (kMode == kSlotKeys) {
                         if (box) {
@@ -422,6 +432,17 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                             tma_load_4d(dst_tile + kRegion, tm_own, 64, hk, r0, b, &full[s]);
                         }
                     }
+                }
+                // Abort: the loads this warp issued must land before the CTA exits.  Only the
+                // last entry armed on each stage can still have loads in flight (an earlier one
+                // was consumed before its stage was armed again), so wait, bounded, for those
+                // phases.  A phase that another warp of the ring never armed cannot complete:
+                // then the CTA holds for a fixed time before it exits instead.
+                if (*abort_flag && armed >= 0) {
+                    bool landed = true;
+                    for (int e = max(0, armed - nst + 1); e <= armed; ++e)
+                        landed = mbar_wait(&full[e % nst], (uint32_t)(e / nst) & 1u, kLandBudget) && landed;
+                    if (!__all_sync(0xffffffffu, landed) && lane == 0) ctl.unlanded = 1;
                 }
             }
         } else {
@@ -459,27 +480,27 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                         umma_ts(d_o, d_s + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (acc || k > 0));
                 };
                 const int e0 = ks.entry(t, 0);
-                bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status) &&
-                          wait_bar(&ctl.k_full[e0 % kKStages], (e0 / kKStages) & 1, abort_flag, dev_status);
+                bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status, budget) &&
+                          wait_bar(&ctl.k_full[e0 % kKStages], (e0 / kKStages) & 1, abort_flag, dev_status, budget);
                 if (ok) {
                     tc_fence_after();
                     issue_s(e0);
                 }
                 for (int i = 0; ok && i < nt; ++i) {
                     const int e = ks.entry(t, i);
-                    ok = wait_bar(&ctl.v_full[e % n_vst], (e / n_vst) & 1, abort_flag, dev_status) &&
-                         wait_bar(&ctl.p_half[t], i & 1, abort_flag, dev_status);
+                    ok = wait_bar(&ctl.v_full[e % n_vst], (e / n_vst) & 1, abort_flag, dev_status, budget) &&
+                         wait_bar(&ctl.p_half[t], i & 1, abort_flag, dev_status, budget);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv_half(e, i > 0, 0);
-                    ok = wait_bar(&ctl.p_full[t], i & 1, abort_flag, dev_status);
+                    ok = wait_bar(&ctl.p_full[t], i & 1, abort_flag, dev_status, budget);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv_half(e, i > 0, 1);
                     umma_commit(&ctl.v_empty[e % n_vst]);
                     if (i + 1 < nt) {
                         const int en = ks.entry(t, i + 1);
-                        ok = wait_bar(&ctl.k_full[en % kKStages], (en / kKStages) & 1, abort_flag, dev_status);
+                        ok = wait_bar(&ctl.k_full[en % kKStages], (en / kKStages) & 1, abort_flag, dev_status, budget);
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(en);
@@ -487,7 +508,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 }
                 // no MMA may still run when TMEM is released
                 umma_commit(&ctl.drain[t]);
-                mbar_wait(&ctl.drain[t], 0, kBudget);
+                mbar_wait(&ctl.drain[t], 0, kDrainBudget);
             }
             __syncwarp();
         }
@@ -519,7 +540,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     drop[cc] = __ballot_sync(0xffffffffu, tk < T_len && rs[tk] == ACACHE_SLOT_NONE);
                 }
             }
-            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], i & 1, abort_flag, dev_status));
+            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], i & 1, abort_flag, dev_status, budget));
             if (!ok) break;
             tc_fence_after();
             // S_t(j) is read into registers as soon as it is ready -- typically while the tensor
@@ -531,7 +552,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             tmem_ld_wait();
             if (pingpong && (t == 1 || i > 0))
                 ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], (t == 0 ? i - 1 : i) & 1,
-                                                      abort_flag, dev_status));
+                                                      abort_flag, dev_status, budget));
             if (!ok) break;
             const int valid = tile_valid<kMode>(p, j, T_len);
             if (valid < kBN) {
@@ -624,7 +645,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
             if (pingpong) mbar_arrive(&ctl.turn[t ^ 1]);
         }
         // drain[t] is committed after the last PV of this chain
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain[t], 0, abort_flag, dev_status));
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain[t], 0, abort_flag, dev_status, budget));
         // Split keys: chain B hands its row maximum and row sum to chain A, which merges the two
         // partial states -- O = O_A 2^(m_A - m) + O_B 2^(m_B - m) with m = max(m_A, m_B), the
         // sums alike -- and stores the rows.  A chain whose keys so far were all discarded has
@@ -641,7 +662,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 ok = false;                                // chain A stores the rows
             } else if (ok) {
                 ok = ctl.split_ok &&
-                     __all_sync(0xffffffffu, wait_bar(&ctl.drain[1], 0, abort_flag, dev_status));
+                     __all_sync(0xffffffffu, wait_bar(&ctl.drain[1], 0, abort_flag, dev_status, budget));
                 const float mb = ctl.split_m[r], lb = ctl.split_l[r];
                 const float m = fmaxf(m_used, mb);
                 w_a = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m);
@@ -731,7 +752,12 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    settle_after_abort(*abort_flag != 0);
+    if (*abort_flag) {
+        // the Q tiles' loads, too, land before the CTA exits
+        if (threadIdx.x == 0 && !mbar_wait(&ctl.q_full, 0, kLandBudget)) ctl.unlanded = 1;
+        __syncthreads();
+        settle_after_abort(ctl.unlanded != 0);
+    }
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
     // A grid of a chain of layers reads nothing its predecessor writes, so it never waited
     // for it; it waits before its CTAs exit instead, so the grids of a chain complete in
@@ -760,6 +786,7 @@ struct ColsumParams {
     int32_t* dev_status;
     int B, P, L, m, Hq, Hkv;
     float scale_log2;
+    long long budget;     // cycles a pipeline wait may take before it gives up
 };
 
 struct ColsumCtl {
@@ -791,6 +818,7 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
+    const long long budget = p.budget;
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.a_full, 1);
@@ -844,8 +872,8 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
             }
             if (c >= kCsStages) {
                 const uint32_t par = ((c / kCsStages) - 1) & 1;
-                if (!__all_sync(0xffffffffu, wait_bar(&ctl.b_empty[s], par, abort_flag, dev_status) &&
-                                                 wait_bar(&ctl.cons_done[s], par, abort_flag, dev_status)))
+                if (!__all_sync(0xffffffffu, wait_bar(&ctl.b_empty[s], par, abort_flag, dev_status, budget) &&
+                                                 wait_bar(&ctl.cons_done[s], par, abort_flag, dev_status, budget)))
                     break;
             }
             // every lane stores its rows' statistics before its arrival on b_full publishes
@@ -885,11 +913,11 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     } else if (warp == kCsMmaWarp) {
         if (lane == 0) {
             const uint32_t id = idesc_bf16(kBN, kBN, false, false);
-            bool ok = wait_bar(&ctl.a_full, 0, abort_flag, dev_status);
+            bool ok = wait_bar(&ctl.a_full, 0, abort_flag, dev_status, budget);
             for (int c = 0; ok && c < n_ch; ++c) {
                 const int s = c % kCsStages, db = c & 1;
-                ok = wait_bar(&ctl.b_full[s], (c / kCsStages) & 1, abort_flag, dev_status);
-                if (ok && c >= 2) ok = wait_bar(&ctl.cons_done[db], ((c >> 1) - 1) & 1, abort_flag, dev_status);
+                ok = wait_bar(&ctl.b_full[s], (c / kCsStages) & 1, abort_flag, dev_status, budget);
+                if (ok && c >= 2) ok = wait_bar(&ctl.cons_done[db], ((c >> 1) - 1) & 1, abort_flag, dev_status, budget);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t sB = base + kTileBytes * (1 + s);
@@ -903,7 +931,7 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
                 umma_commit(&ctl.b_empty[s]);
             }
             umma_commit(&ctl.drain);
-            mbar_wait(&ctl.drain, 0, kBudget);
+            mbar_wait(&ctl.drain, 0, kDrainBudget);
         }
         __syncwarp();
     } else {
@@ -918,8 +946,8 @@ tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
             const int s = c % kCsStages, db = c & 1;
             // the stats of this chunk were published with b_full; D with d_full
             ok = __all_sync(0xffffffffu,
-                            wait_bar(&ctl.b_full[s], (c / kCsStages) & 1, abort_flag, dev_status) &&
-                            wait_bar(&ctl.d_full[db], (c >> 1) & 1, abort_flag, dev_status));
+                            wait_bar(&ctl.b_full[s], (c / kCsStages) & 1, abort_flag, dev_status, budget) &&
+                            wait_bar(&ctl.d_full[db], (c >> 1) & 1, abort_flag, dev_status, budget));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -997,6 +1025,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
+    const long long budget = p.budget;
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 32);
@@ -1084,7 +1113,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
             const int s = i % kCrKStages;
             if (i >= kCrKStages &&
                 !__all_sync(0xffffffffu,
-                            wait_bar(&ctl.k_empty[s], ((i / kCrKStages) - 1) & 1, abort_flag, dev_status)))
+                            wait_bar(&ctl.k_empty[s], ((i / kCrKStages) - 1) & 1, abort_flag, dev_status, budget)))
                 break;
             if (lane == 0) {
                 const int j0 = (jt0 + i) * kBN;
@@ -1097,11 +1126,11 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
     } else if (warp == kCrMmaWarp) {
         if (lane == 0) {
             const uint32_t id = idesc_bf16(kBN, kBN, false, false);
-            bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
+            bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status, budget);
             for (int i = 0; ok && i < n_t; ++i) {
                 const int ks = i % kCrKStages, db = i & 1;     // key stage, D buffer
-                ok = wait_bar(&ctl.k_full[ks], (i / kCrKStages) & 1, abort_flag, dev_status);
-                if (ok && i >= 2) ok = wait_bar(&ctl.cons_done[db], ((i >> 1) - 1) & 1, abort_flag, dev_status);
+                ok = wait_bar(&ctl.k_full[ks], (i / kCrKStages) & 1, abort_flag, dev_status, budget);
+                if (ok && i >= 2) ok = wait_bar(&ctl.cons_done[db], ((i >> 1) - 1) & 1, abort_flag, dev_status, budget);
                 if (!ok) break;
                 tc_fence_after();
                 for (int c = 0; c < n_ch; ++c) {
@@ -1116,7 +1145,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
                 umma_commit(&ctl.k_empty[ks]);
             }
             umma_commit(&ctl.drain);
-            mbar_wait(&ctl.drain, 0, kBudget);
+            mbar_wait(&ctl.drain, 0, kDrainBudget);
         }
         __syncwarp();
     } else {
@@ -1124,10 +1153,10 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
         const int r = threadIdx.x & 127;                   // affix key r of every tile
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float c2 = p.scale_log2;
-        bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
+        bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status, budget);
         for (int i = 0; i < n_t; ++i) {
             const int s = i & 1;
-            ok = ok && wait_bar(&ctl.d_full[s], (i >> 1) & 1, abort_flag, dev_status);
+            ok = ok && wait_bar(&ctl.d_full[s], (i >> 1) & 1, abort_flag, dev_status, budget);
             // both warpgroups take the same decision, so neither waits for the other in vain
             ok = named_barrier_and<1>(256, ok);
             if (!ok) break;
@@ -1227,6 +1256,7 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     prm.Hkv = a.hkv;
     prm.T_len = T_len;
     prm.scale_log2 = a.scale * kLog2e;
+    prm.budget = wait_budget();
     return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream, pdl || chained)
                      : launch_attn<kSlotKeys>(prm, B, stream, pdl || chained);
 }
@@ -1257,6 +1287,7 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
     prm.Hkv = a.hkv;
     prm.T_len = max_T;
     prm.scale_log2 = a.scale * kLog2e;
+    prm.budget = wait_budget();
     return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream) : launch_attn<kSlotKeys>(prm, B, stream);
 }
 
@@ -1288,6 +1319,7 @@ int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, co
     prm.L = L;
     prm.P = P;
     prm.scale_log2 = a.scale * kLog2e;
+    prm.budget = wait_budget();
     return launch_attn<kProbeKeys>(prm, B, stream);
 }
 
@@ -1323,6 +1355,7 @@ int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
     prm.scale_log2 = a.scale * kLog2e;
+    prm.budget = wait_budget();
     if ((m + kBN - 1) / kBN <= kCrMaxChunks) {
         // masked rows resident: one CTA per (request, head) and run of affix tiles, the runs
         // as long as the SMs allow (one CTA per SM)

@@ -68,7 +68,7 @@ constexpr uint32_t kSmemBytes = kTileBytes * (1 + 2 * kStages) + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColO = 256, kColP0 = 384;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr long long kBudget = 1LL << 31;
+constexpr long long kDrainBudget = 1LL << 31;   // cycles: MMAs issued before an abort
 
 struct DecParams {
     CUtensorMap tm_q;     // 4-D [B][n_q][Hq][d], box {64, g, qpb, 1}
@@ -83,6 +83,7 @@ struct DecParams {
     int n_rb;             // row blocks per (request, KV head)
     int cs;               // CTAs per cluster (key-range split)
     float scale_log2;
+    long long budget;     // cycles a pipeline wait may take before it gives up
 };
 
 struct DecCtl {
@@ -99,13 +100,14 @@ struct DecCtl {
     float part_l[kBM];    // per TMEM lane: row sum
 };
 
-ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* dev_status) {
+ACACHE_DEVFN bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* dev_status,
+                           long long budget) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kBudget) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             flag(dev_status, ACACHE_DEV_TIMEOUT);
             return false;
@@ -144,6 +146,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
+    const long long budget = p.budget;
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl.q_full, 1);
@@ -229,7 +232,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
                 int rows[4] = {next[0], next[1], next[2], next[3]};
                 resolve(j + 1, next);
                 if (j >= kStages &&
-                    !__all_sync(0xffffffffu, wait_bar(&empty[s], ((j / kStages) - 1) & 1, abort_flag, dev_status)))
+                    !__all_sync(0xffffffffu, wait_bar(&empty[s], ((j / kStages) - 1) & 1, abort_flag, dev_status, budget)))
                     break;
                 if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
                 __syncwarp();
@@ -258,16 +261,16 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
                     umma_commit(&ctl.s_full[j & 1]);
                     umma_commit(&ctl.k_empty[j % kStages]);
                 };
-                ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status);
+                ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status, budget);
                 for (int j = 0; ok && j < 2 && j < n_kv; ++j) {
-                    ok = wait_bar(&ctl.k_full[j], 0, abort_flag, dev_status);
+                    ok = wait_bar(&ctl.k_full[j], 0, abort_flag, dev_status, budget);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j);
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
-                    ok = wait_bar(&ctl.v_full[j % kStages], (j / kStages) & 1, abort_flag, dev_status) &&
-                         wait_bar(&ctl.p_full[j & 1], (j >> 1) & 1, abort_flag, dev_status);
+                    ok = wait_bar(&ctl.v_full[j % kStages], (j / kStages) & 1, abort_flag, dev_status, budget) &&
+                         wait_bar(&ctl.p_full[j & 1], (j >> 1) & 1, abort_flag, dev_status, budget);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t dv = sdesc_sw128(sV(j % kStages), kRegion, 1024);
@@ -278,14 +281,14 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
                     umma_commit(&ctl.v_empty[j % kStages]);
                     umma_commit(&ctl.pv_done);
                     if (j + 2 < n_kv) {
-                        ok = wait_bar(&ctl.k_full[(j + 2) % kStages], ((j + 2) / kStages) & 1, abort_flag, dev_status);
+                        ok = wait_bar(&ctl.k_full[(j + 2) % kStages], ((j + 2) / kStages) & 1, abort_flag, dev_status, budget);
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(j + 2);
                     }
                 }
                 umma_commit(&ctl.drain);
-                mbar_wait(&ctl.drain, 0, kBudget);
+                mbar_wait(&ctl.drain, 0, kDrainBudget);
             }
             __syncwarp();
         }
@@ -321,7 +324,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
                     drop[cc] = __ballot_sync(0xffffffffu, tk < p.T_len && rs[tk] == ACACHE_SLOT_NONE);
                 }
             }
-            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[sb], (j >> 1) & 1, abort_flag, dev_status));
+            ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[sb], (j >> 1) & 1, abort_flag, dev_status, budget));
             if (!ok) break;
             tc_fence_after();
             uint32_t v[NC][32];
@@ -369,7 +372,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
             }
             if (__any_sync(0xffffffffu, resc)) {
                 // O holds tiles 0..j-1 once PV(j-1) has completed
-                ok = __all_sync(0xffffffffu, wait_bar(&ctl.pv_done, (j - 1) & 1, abort_flag, dev_status));
+                ok = __all_sync(0xffffffffu, wait_bar(&ctl.pv_done, (j - 1) & 1, abort_flag, dev_status, budget));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -408,7 +411,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
             tc_fence_before();
             mbar_arrive(&ctl.p_full[sb]);
         }
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain, 0, abort_flag, dev_status));
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain, 0, abort_flag, dev_status, budget));
         if (ok) {
             tc_fence_after();
             if (REP == 1 && cs == 1) {
@@ -660,6 +663,7 @@ int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q,
     prm.n_rb = dg.n_rb;
     prm.cs = dg.cs;
     prm.scale_log2 = a.scale * kLog2e;
+    prm.budget = wait_budget();
     if (drop_none) {
         switch (dg.rep) {
             case 4: return launch_rep<4, true>(prm, ctas, stream, pdl);

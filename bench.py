@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the block-decode measurement")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the compact per-launch record of the other workloads in the JSON line")
     ap.add_argument("--sweep", action="store_true",
                     help="per-launch measurements of the other workloads (Dream GQA infix, paged "
                          "LLaDA decode, long suffix with its ratio and batch sweeps), one JSON line each")
@@ -575,15 +577,14 @@ def _launch_set(path):
     return probe, write, slot
 
 
-def sweep(args):
+def sweep_records(peaks, dev, full=True):
     """Per-launch measurements of the workloads other than the headline one.  Four layers are
     materialised per workload (all layers have the same shapes, so a launch's time does not
     depend on which layer it runs); whole-pass times are the per-launch times times the
-    launch counts and are labelled as such."""
-    peaks = measured_peaks()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
+    launch counts and are labelled as such.  full=False keeps the record compact: the long
+    suffix's slot attention at batch 1, 4 and 32 only, and the decode figures in brief."""
     peak = peaks["bf16_tflops_sustained"]
+    out = []
     for name, ratios in ((wl.DREAM_INFIX.name, (200,)), (wl.LLADA_PAGED.name, (200,)),
                          (wl.LLADA_SUFFIX.name, (100, 200, 300))):
         base = wl.CATALOGUE[name]
@@ -595,10 +596,11 @@ def sweep(args):
             probe_ms, write_ms, slot_ms = _launch_set(path)
             row = w.hkv * w.d * w.esize
             slot_tf = slot_flops_per_launch(w) / (slot_ms / 1e3) / 1e12
+            probe_tf = probe_flops(w) / w.layers / (probe_ms / 1e3) / 1e12
             line = {"sweep": name, "ratio": ratio / 1000, "K": w.K, "R": w.R, "batch": w.batch, "T": w.T,
                     "layers_full": base.layers, "recompute_points_full": base.recompute_points,
-                    "probe_ms_per_layer": probe_ms,
-                    "probe_tflops": probe_flops(w) / w.layers / (probe_ms / 1e3) / 1e12,
+                    "probe_ms_per_layer": probe_ms, "probe_tflops": probe_tf,
+                    "probe_frac_of_peak": probe_tf / peak,
                     "slot_attn_ms_per_launch": slot_ms, "slot_attn_tflops": slot_tf,
                     "slot_attn_frac_of_peak": slot_tf / peak,
                     "write_ms_per_launch": write_ms,
@@ -606,8 +608,11 @@ def sweep(args):
                     "anchor_scored_tokens_per_s_est": w.batch * w.L / (base.layers * probe_ms / 1e3),
                     "full_pass_ms_est": base.layers * probe_ms + base.recompute_points * base.layers * (write_ms + slot_ms),
                     "peak": {"bf16_tflops_sustained": peak, "hbm_gbs": peaks["hbm_gbs"], "source": peaks["source"]}}
-            if name == wl.LLADA_PAGED.name or (name == wl.DREAM_INFIX.name):
-                line["decode"] = Decode(path).measure(5, 2, peaks)
+            if name in (wl.LLADA_PAGED.name, wl.DREAM_INFIX.name):
+                dec = Decode(path).measure(5, 2, peaks)
+                line["decode"] = dec if full else {
+                    "attn_ms_per_launch": dec["attn_ms_per_launch"], "write_ms_per_launch": dec["write_ms_per_launch"],
+                    "unique_gbs": dec["roofline"]["achieved"], "frac_of_hbm": dec["roofline"]["frac"]}
             if name == wl.LLADA_SUFFIX.name and ratio == 200:
                 one = Path(w.replace(batch=1), dev)
                 one.step()
@@ -615,16 +620,27 @@ def sweep(args):
                 line["probe_ms_per_request_batch1"] = base.layers * p1
                 del one
                 vs = {}
-                for b in (1, 2, 4, 8, 16, 32):
+                for b in ((1, 2, 4, 8, 16, 32) if full else (1, 4, 32)):
+                    if b == w.batch:
+                        vs[b] = slot_tf
+                        continue
                     pb = Path(w.replace(batch=b, layers=1), dev)
                     pb.step()
                     _, _, sb = _launch_set(pb)
                     vs[b] = slot_flops_per_launch(pb.w) / (sb / 1e3) / 1e12
                     del pb
                 line["slot_attn_tflops_vs_batch"] = vs
-            print(json.dumps(line), flush=True)
+            out.append(line)
             del path
             torch.cuda.empty_cache()
+    return out
+
+
+def sweep(args):
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for line in sweep_records(measured_peaks(), dev):
+        print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------------------- main
@@ -650,19 +666,79 @@ def reduce_max(x, device=None):
     return float(t.item())
 
 
+def host_cpu():
+    """The host's CPU: os.cpu_count() and the model name lscpu reports (None if unknown)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"cpu_count": os.cpu_count(), "model": model}
+
+
+def oracle_sample_step(w, layer, rows_per_layer=64, layers=4):
+    """One reference-arm step: a bounded sample of the workload for the oracle -- request 0,
+    `layers` consecutive layers from `layer` on, each the probe of all heads and the slot
+    attention of the first `rows_per_layer` recomputed rows.  Returns (flops, seconds)."""
+    import numpy as np
+    import oracle
+    w1 = w.replace(batch=1)
+    lay = wl.slot_layout(w1)
+    masked = w.masked_rows()
+    flops, secs = 0.0, 0.0
+    for i in range(layers):
+        n = (layer + i) % w.layers
+        p = wl.probe_inputs(w1, n)
+        r = wl.recompute_inputs(w1, n)
+        anchors = np.arange(w.K, dtype=np.int32)[None]
+        _, rs = oracle.build_slot_maps(anchors, lay.shared_slot, lay.private_slots, T=w.T, l=w.l, L=w.L)
+        kc = torch.zeros((lay.num_slots, w.hkv, w.d), dtype=w.torch_dtype)
+        vc = torch.zeros_like(kc)
+        kc[lay.private_slots[0].long()], vc[lay.private_slots[0].long()] = r["k_new"][0], r["v_new"][0]
+        kc[lay.shared_slot.long()], vc[lay.shared_slot.long()] = p["k_aff"], p["v_aff"]
+        rows = list(range(min(rows_per_layer, w.R)))
+        t0 = time.perf_counter()
+        oracle.probe_layer(p["q"], p["k_req"], p["v_req"], p["k_aff"], p["v_aff"], T=w.T, l=w.l,
+                           masked_rows=masked, scale=w.scale)
+        oracle.slot_attention(r["q_r"], rs, kc, vc, scale=w.scale, rows=rows)
+        secs += time.perf_counter() - t0
+        flops += probe_flops(w1) / w.layers + 4.0 * len(rows) * w.T * w.d * w.hq
+    return flops, secs
+
+
 def run_reference(args, w, world, rank):
+    """The reference arm: the float64 CPU oracle, as it stands, on the host cores.  A step is a
+    bounded sample of the workload (oracle_sample_step); W untimed steps, then K timed ones."""
     if rank != 0:
         return
-    flops, secs, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
+    import oracle
+    layers_per_step = 4
+    for k in range(args.warmup):
+        oracle_sample_step(w, k * layers_per_step, layers=layers_per_step)
+    flops, secs = 0.0, 0.0
+    for k in range(args.steps):
+        f, t = oracle_sample_step(w, (args.warmup + k) * layers_per_step, layers=layers_per_step)
+        flops += f
+        secs += t
     v = flops / secs / 1e12
-    per_step_s = secs
+    cores = oracle.get_threads()
+    sample = (f"one step = request 0 of the workload, {layers_per_step} layers, each the probe of all "
+              f"{w.hq} heads over P = {w.P} rows and the slot attention of the first 64 of R = {w.R} "
+              f"recomputed rows ({flops / args.steps / 1e9:.1f} GFLOP per step)")
     line = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_s * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "step": "a bounded sample of the workload (see cpu_baseline.sample), not a full step",
+            "ms_per_full_step_extrapolated": step_flops(w) / (v * 1e12) * 1e3,
+            "extrapolation": "the full step's algorithmic FLOPs divided by the measured sample rate",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, shapes of the LLaDA-8B prefix workload)",
             "config": {"workload": w.name, **{k: v2 for k, v2 in w.describe().items() if k != "workload"}},
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "sample": sample, **host_cpu()},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -750,6 +826,11 @@ def main():
         up_after = path.upload_ms()
         e2e = {"value": step_flops(w) * n_e2e * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n_e2e,
+               "uploaded": "every layer's probe Q and own K/V rows, and every layer's recompute-point Q and "
+                           "fresh K/V (the shared affix cache is resident)",
+               "read_back": "the step's importance scores, its anchors and the last layer's read-slot "
+                            "attention output; the other layers' outputs stay on the device, where a "
+                            "decoding engine consumes them",
                "ms_per_step": ems / n_e2e, "upload_ms_per_step": [up_ms, up_after],
                "h2d_gbs": [bi / (up_ms / 1e3) / 1e9, bi / (up_after / 1e3) / 1e9]}
 
@@ -759,11 +840,18 @@ def main():
     fused = store_attend_compare(path)
     copies = copy_bandwidth(path, peaks)
 
+    others = None
+    if world == 1 and not args.no_sweep:
+        t0 = time.perf_counter()
+        others = {"timing": "CUDA events per launch, 4 materialised layers per workload (see sweep_records)",
+                  "records": sweep_records(peaks, dev, full=False)}
+        others["seconds"] = time.perf_counter() - t0
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         flops, secs, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": desc}
+               "sample": desc, **host_cpu()}
 
     if rank == 0:
         gb_touched = sum(t.numel() * t.element_size() for p in path.probe for t in p.values()) + \
@@ -790,6 +878,7 @@ def main():
             "store_then_attend": {"timing": "CUDA events, one recompute point over all layers, 3 passes",
                                   **fused},
             "copies": {"timing": "CUDA events, every layer, 3 passes", **copies},
+            "other_workloads": others,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": path.launches_per_step * args.steps,

@@ -78,7 +78,9 @@ enum {
 typedef struct {
     int32_t num_q_heads;    /* Hq                                                    */
     int32_t num_kv_heads;   /* Hkv, Hq % Hkv == 0; query head h reads KV head h/(Hq/Hkv) */
-    int32_t head_dim;       /* d: 64 or 128                                          */
+    int32_t head_dim;       /* d: 64 or 128.  The tensor-core kernels cover bf16 at 128;
+                               float32 (either d) and bf16 at d = 64 run on CUDA cores
+                               (same results and errors, far lower throughput)      */
     float scale;            /* softmax scale, normally 1/sqrt(d) (Eq. 4)             */
     int32_t dtype;          /* acache_dtype of Q, K, V and O                         */
 } acache_attn_desc;
@@ -87,6 +89,18 @@ typedef struct {
 ACACHE_API const char* acache_status_string(int status);
 /* Library version: major*10000 + minor*100 + patch. */
 ACACHE_API int acache_version(void);
+
+/* ---------------------------------------------------------------------------------
+ * Failure detection: the budget of the kernels' bounded waits (host, thread-safe).
+ * Every wait of a tensor-core kernel's pipeline (a TMA load, an MMA, another role's hand-off)
+ * gives up after `budget` SM clock cycles: the kernel then sets ACACHE_DEV_TIMEOUT in
+ * dev_status, stops its work (its outputs are not written), lets the copies and MMAs it had
+ * issued finish, releases its tensor memory and exits, so the context stays usable.  The
+ * page has no counterpart: this is the library's own watchdog.
+ * cycles > 0 sets the budget of kernels launched after the call; cycles <= 0 only reads it.
+ * Returns the budget in force before the call (default 2^31 cycles, about 1 s at 2.07 GHz).
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int64_t acache_wait_budget(int64_t cycles);
 
 /* ---------------------------------------------------------------------------------
  * (1)+(2) Anchor probe of ONE layer and its importance contribution.
@@ -132,8 +146,10 @@ ACACHE_API int acache_probe_scores(const acache_attn_desc* a, int batch, int seq
  * process exits.  A call needing more than that (2 * round256(B*Hq*P*4) +
  * round256(B*Hq*L*4) bytes) returns ACACHE_ERR_WORKSPACE and launches nothing.  The call
  * allocates nothing (no cudaMalloc/cudaFree, no allocating library routine).
- *  - The first call on a device looks up the array's device address (once per device,
- *    with that device current); make that first call before any stream capture starts.
+ *  - Every call made while `stream` is not capturing looks up the array's device address on
+ *    the current device (so the entry point keeps working after a device reset); a call made
+ *    during stream capture reuses the address found by the device's last earlier call, so
+ *    make the first call on each device before any stream capture starts.
  *  - All calls share the array and it keeps the last call's contents.  Nothing in it must
  *    start at zero (each call writes every scratch byte it reads), but calls whose kernels
  *    can overlap on the GPU (unordered streams) race on it: order them.

@@ -27,8 +27,19 @@ def test_library_exports_every_declared_symbol():
     L = ac.lib()
     for n in names:
         assert getattr(L, n) is not None
-    assert ac.version() == 100
+    assert ac.version() == 200
     assert ac.status_string(0) == "ok"
+
+
+def test_wait_budget_set_and_read_on_the_host():
+    # host-side state only: no kernel is launched
+    default = ac.acache_wait_budget()
+    assert default == 1 << 31
+    assert ac.acache_wait_budget(12345) == default
+    assert ac.acache_wait_budget(0) == 12345          # <= 0 reads without setting
+    assert ac.acache_wait_budget(-7) == 12345
+    assert ac.acache_wait_budget(default) == 12345
+    assert ac.acache_wait_budget() == default
 
 
 def test_struct_layout_matches_header():

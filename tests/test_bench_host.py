@@ -38,7 +38,11 @@ def test_reference_arm_single_rank():
     d = lines[0]
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["cpu_count"] >= 1 and "model" in d["cpu_baseline"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "tiny_prefix_f32"
+    # the steps the line claims are the steps it ran: each a bounded sample, timed
+    assert d["steps"] == 1 and d["warmup"] == 0 and d["ms_per_step"] > 0
+    assert "sample" in d["step"] and d["ms_per_full_step_extrapolated"] > 0
 
 
 def test_reference_arm_two_gloo_ranks_prints_once():

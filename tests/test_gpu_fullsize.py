@@ -23,6 +23,11 @@ pytestmark = pytest.mark.gpu
 
 FULL = [wl.LLADA_PREFIX, wl.DREAM_INFIX, wl.LLADA_PAGED, wl.LLADA_SUFFIX]
 IDS = [w.name for w in FULL]
+# the long-suffix workload's anchor-ratio sweep (0.1 and 0.3 besides the default 0.2): K and R
+# change, and with them the recomputed query rows' tiling and the private pages
+RATIO_SWEEP = [wl.LLADA_SUFFIX.replace(ratio_permille=r) for r in (100, 300)]
+STORE_ATTEND = FULL + RATIO_SWEEP
+STORE_ATTEND_IDS = IDS + [f"{w.name}_ratio{w.ratio_permille / 1000:g}" for w in RATIO_SWEEP]
 
 
 def sample_rows(n, seed, count=12):
@@ -69,7 +74,7 @@ def test_fullsize_probe_layer(w):
     assert np.array_equal(anchors.cpu().numpy(), want)
 
 
-@pytest.mark.parametrize("w", FULL, ids=IDS)
+@pytest.mark.parametrize("w", STORE_ATTEND, ids=STORE_ATTEND_IDS)
 def test_fullsize_store_and_slot_attention(w):
     lay = wl.slot_layout(w)
     inp = wl.probe_inputs(w, 0, device="cuda")
