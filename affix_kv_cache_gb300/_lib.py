@@ -29,7 +29,7 @@ DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOU
 DEV_BAD_LENGTH = 64
 
 EXPORTS = ("acache_status_string", "acache_version", "acache_wait_budget", "acache_probe_workspace_bytes",
-           "acache_probe_scores", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
+           "acache_probe_scores", "acache_probe_scores_layers", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
            "acache_write_slots", "acache_slot_attention", "acache_gather_slots",
            "acache_kv_deviation_scores", "acache_slot_attention_dropna", "acache_slot_attention_varlen",
            "acache_store_attend", "acache_store_attend_layers", "acache_rerotate_keys", "acache_pool_create",
@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
             "acache_wait_budget": (I64, [I64]),
             "acache_probe_workspace_bytes": (S, [D, I, I, I, I]),
             "acache_probe_scores": (I, [D, I, I, I, I, P, I, P, P, P, P, P, P, P, P, S, P, P]),
+            "acache_probe_scores_layers": (I, [D, I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, S, P, P]),
             "acache_probe_scores_noalloc": (I, [D, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P]),
             "acache_topk_anchors": (I, [P, I, I, I, P, P, P]),
             "acache_build_slot_maps": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
@@ -157,6 +158,24 @@ def acache_probe_scores(desc, batch, seq_len, affix_begin, affix_len, masked_row
                                    _p(k_affix), _p(v_affix), _p(out), _p(scores), _p(workspace),
                                    workspace_bytes, _p(dev_status), _stream(stream))
     return _check("acache_probe_scores", st) if check else st
+
+
+def acache_probe_scores_layers(desc, batch, seq_len, affix_begin, affix_len, masked_rows, num_masked,
+                               q, k_req, v_req, k_affix, v_affix, out, scores, workspace,
+                               workspace_bytes=None, dev_status=None, stream=None, check=True):
+    """The probe of every layer in one call (see include/acache.h): q, k_req, v_req, k_affix,
+    v_affix and out are lists of tensors, one per layer (out, k_affix and v_affix may be None)."""
+    layers = len(q)
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    keep = [_ptr_array(x, layers) for x in (q, k_req, v_req, k_affix, v_affix, out)]
+    ptrs = [k[0] if k is not None else None for k in keep]
+    st = lib().acache_probe_scores_layers(ctypes.byref(desc), layers, batch, seq_len, affix_begin, affix_len,
+                                          _p(masked_rows), num_masked, ptrs[0], ptrs[1], ptrs[2], ptrs[3],
+                                          ptrs[4], ptrs[5], _p(scores), _p(workspace), workspace_bytes,
+                                          _p(dev_status), _stream(stream))
+    del keep
+    return _check("acache_probe_scores_layers", st) if check else st
 
 
 def acache_probe_scores_noalloc(desc, batch, seq_len, affix_begin, affix_len, masked_rows,
@@ -242,12 +261,12 @@ def acache_slot_attention_varlen(desc, batch, q_start, max_q_rows, total_q_rows,
 
 
 def _ptr_array(ts, n):
-    """Host array of n device pointers (None when ts is None)."""
+    """Host array of n device pointers (None when ts is None; a None entry is a null pointer)."""
     if ts is None:
         return None
     if len(ts) != n:
         raise ValueError(f"expected {n} per-layer tensors, got {len(ts)}")
-    arr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+    arr = (ctypes.c_void_p * n)(*[None if t is None else t.data_ptr() for t in ts])
     return ctypes.cast(arr, ctypes.c_void_p), arr
 
 

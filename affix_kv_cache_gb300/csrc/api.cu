@@ -3,8 +3,10 @@
 #include <math.h>
 
 #include <atomic>
+#include <vector>
 
 #include "attn.cuh"
+#include "ptx.cuh"
 #include "tc_attn.cuh"
 
 namespace acache {
@@ -74,9 +76,13 @@ ProbeWorkspace carve_probe_ws(void* base, int64_t B, int64_t Hq, int64_t P, int6
     return w;
 }
 
-// scores[b][j] += sum over heads h (ascending) of partial[b][h][j]
+// scores[b][j] += sum over heads h (ascending) of partial[b][h][j].  Launched behind the mass
+// pass (programmatic dependent launch): it waits for it before reading the partial sums, and
+// lets the next layer's probe forward start at once.
 __global__ void score_reduce_kernel(int B, int Hq, int L, const float* __restrict__ partial,
                                     float* __restrict__ scores) {
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid >= (int64_t)B * L) return;
     const int64_t b = gid / L, j = gid % L;
@@ -91,7 +97,19 @@ int launch_score_reduce(int B, int Hq, int L, const float* partial, float* score
                         cudaStream_t stream) {
     const int64_t n = (int64_t)B * L;
     if (n == 0) return ACACHE_OK;
-    score_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(B, Hq, L, partial, scores);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((n + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, score_reduce_kernel, B, Hq, L, partial, scores) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ACACHE_ERR_CUDA;
+    }
     return launch_status();
 }
 
@@ -160,7 +178,7 @@ int probe_launch(const ProbeCall& c, void* scratch, int32_t* dev_status, cudaStr
     int rc;
     if (tc_supported(a)) {
         rc = launch_tc_probe_pass_a(a, c.B, c.T, c.l, c.L, c.q, c.k_req, c.v_req, c.k_aff, c.v_aff, c.out,
-                                    ws.stat_m, ws.stat_l, dev_status, stream);
+                                    ws.stat_m, ws.stat_l, dev_status, stream, c.chained);
     } else {
         rc = launch_simt_probe_pass_a(a, c.B, c.T, c.l, c.L, c.q, c.k_req, c.v_req, c.k_aff, c.v_aff, c.out,
                                       ws.stat_m, ws.stat_l, stream);
@@ -225,6 +243,61 @@ int acache_probe_scores(const acache_attn_desc* desc, int batch, int seq_len, in
     if (!workspace || workspace_bytes < probe_scratch_bytes(c)) return ACACHE_ERR_WORKSPACE;
     if ((uintptr_t)workspace & 255u) return ACACHE_ERR_INVALID_ARG;
     return probe_launch(c, workspace, dev_status, (cudaStream_t)stream_);
+}
+
+int acache_probe_scores_layers(const acache_attn_desc* desc, int layers, int batch, int seq_len,
+                               int affix_begin, int affix_len, const int32_t* masked_rows, int num_masked,
+                               const void* const* q, const void* const* k_req, const void* const* v_req,
+                               const void* const* k_affix, const void* const* v_affix, void* const* out,
+                               float* scores, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               void* stream_) {
+    if (layers < 0) return ACACHE_ERR_INVALID_ARG;
+    if (layers == 0) return ACACHE_OK;
+    if (!q || !k_req || !v_req || (affix_len > 0 && (!k_affix || !v_affix))) return ACACHE_ERR_INVALID_ARG;
+    // every layer's arguments are checked before anything is launched
+    std::vector<ProbeCall> calls((size_t)layers);
+    bool empty = false;
+    for (int n = 0; n < layers; ++n)
+        if (int rc = probe_check(desc, batch, seq_len, affix_begin, affix_len, masked_rows, num_masked, q[n],
+                                 k_req[n], v_req[n], k_affix ? k_affix[n] : nullptr,
+                                 v_affix ? v_affix[n] : nullptr, out ? out[n] : nullptr, scores,
+                                 &calls[(size_t)n], &empty))
+            return rc;
+    if (empty) return ACACHE_OK;
+    const ProbeCall& c0 = calls[0];
+    if (!workspace || workspace_bytes < probe_scratch_bytes(c0)) return ACACHE_ERR_WORKSPACE;
+    if ((uintptr_t)workspace & 255u) return ACACHE_ERR_INVALID_ARG;
+    // A chained forward reads its layer's inputs before the grids ahead of it are complete:
+    // chain only when nothing the call writes (any layer's output, the scores, the workspace)
+    // meets any layer's inputs.
+    const int64_t eb = elem_bytes(c0.a.dtype), P = c0.T - c0.L;
+    const int64_t qo_bytes = (int64_t)c0.B * P * c0.a.hq * c0.a.d * eb;
+    const int64_t req_bytes = (int64_t)c0.B * P * c0.a.hkv * c0.a.d * eb;
+    const int64_t aff_bytes = (int64_t)c0.L * c0.a.hkv * c0.a.d * eb;
+    struct Range {
+        uintptr_t lo, hi;
+    };
+    auto span = [](const void* ptr, int64_t bytes) {
+        return Range{(uintptr_t)ptr, ptr ? (uintptr_t)ptr + (uintptr_t)bytes : (uintptr_t)ptr};
+    };
+    std::vector<Range> written = {span(scores, (int64_t)c0.B * c0.L * 4),
+                                  span(workspace, (int64_t)probe_scratch_bytes(c0))};
+    for (const ProbeCall& c : calls) written.push_back(span(c.out, qo_bytes));
+    bool disjoint = true;
+    for (const ProbeCall& c : calls) {
+        const Range read[5] = {span(c.q, qo_bytes), span(c.k_req, req_bytes), span(c.v_req, req_bytes),
+                               span(c.k_aff, aff_bytes), span(c.v_aff, aff_bytes)};
+        for (const Range& x : written)
+            for (const Range& y : read)
+                if (x.lo < x.hi && y.lo < y.hi && x.lo < y.hi && y.lo < x.hi) disjoint = false;
+    }
+    cudaStream_t st = (cudaStream_t)stream_;
+    for (int n = 0; n < layers; ++n) {
+        ProbeCall& c = calls[(size_t)n];
+        c.chained = disjoint && n > 0;
+        if (int rc = probe_launch(c, workspace, dev_status, st)) return rc;
+    }
+    return ACACHE_OK;
 }
 
 int acache_topk_anchors(const float* scores, int batch, int affix_len, int k, int32_t* anchors,

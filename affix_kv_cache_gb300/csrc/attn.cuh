@@ -103,6 +103,7 @@ struct ProbeCall {
     const void *q, *k_req, *v_req, *k_aff, *v_aff;
     void* out;
     float* scores;
+    bool chained = false;   // a later layer of acache_probe_scores_layers (programmatic launch)
 };
 // Validates a probe call's arguments (errors as acache_probe_scores); on ACACHE_OK, *empty
 // says there is nothing to launch, else *c holds the call.

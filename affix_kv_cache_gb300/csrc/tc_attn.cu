@@ -115,7 +115,12 @@ struct AttnParams {
     float* stat_l;
     int32_t* dev_status;
     int64_t num_slots;
-    int early_wait;       // 1: the pool may have been written by the grid this one follows
+    // when the grid waits for the grid it follows on the stream (programmatic dependent launch):
+    // 1 before any K/V load (the pool may have been written by it: store-then-attend), 0 only
+    // before its CTAs exit (a chained layer: it reads nothing its predecessor writes), 2 before
+    // its first global write (the probe forward of the next layer: it writes the scratch the
+    // preceding grids of the probe read)
+    int early_wait;
     int n_rows, Hq, Hkv, T_len, L, P;
     float scale_log2;
     long long budget;     // cycles a pipeline wait may take before it gives up
@@ -385,7 +390,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 // Only then may the next grid on the stream start: in a chain of layers it runs on
                 // the SMs this grid's last wave leaves idle, and reads its own layer's pool
                 // without waiting (that store is complete once this wait returns).
-                if (p.early_wait) grid_dependency_wait();
+                if (p.early_wait == 1) grid_dependency_wait();
                 grid_launch_dependents();
                 int armed = -1;                           // last entry this warp arrived on
                 for (int e = 0; e < n_kv; ++e) {          // ring entries in load order
@@ -671,6 +676,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 m_used = m;
             }
         }
+        // the grids this one follows may still read the scratch it writes: wait for them
+        if (p.early_wait == 2) grid_dependency_wait();
         // Output rows leave through this chain's Q buffer, free once its MMAs (and with split
         // keys chain B's) are complete, and two tensor-map stores of whole 256-byte row slices,
         // instead of per-thread 16-byte stores scattered at the query-row stride.  A ragged
@@ -762,8 +769,10 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     // A grid of a chain of layers reads nothing its predecessor writes, so it never waited
     // for it; it waits before its CTAs exit instead, so the grids of a chain complete in
     // launch order and work behind the chain on the stream sees every layer's output.  (The
-    // predecessor has long finished by then: this grid started in its last wave.)
-    if (!p.early_wait && threadIdx.x == 0) grid_dependency_wait();
+    // predecessor has long finished by then: this grid started in its last wave.)  A chained
+    // probe forward waited before its epilogue; a CTA that gave up a wait and skipped it waits
+    // here, so that its grid still completes after the ones it follows.
+    if (p.early_wait != 1 && threadIdx.x == 0) grid_dependency_wait();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -806,6 +815,10 @@ __global__ void __launch_bounds__(kCsThreads, 2)
 tc_colsum_kernel(const __grid_constant__ ColsumParams p) {
     extern __shared__ uint8_t dsm[];
     __shared__ ColsumCtl ctl;
+    // launched behind the probe forward (programmatic dependent launch): its row statistics are
+    // read below; the head sum after this grid may start waiting now
+    grid_launch_dependents();
+    grid_dependency_wait();
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     const uint32_t sA = base;
     const int n_jt = (p.L + kBN - 1) / kBN;
@@ -1009,6 +1022,10 @@ __global__ void __launch_bounds__(kCrThreads, 1)
 tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta) {
     extern __shared__ uint8_t dsm[];
     __shared__ ColsumRowsCtl ctl;
+    // launched behind the probe forward (programmatic dependent launch): its row statistics are
+    // read below; the head sum after this grid may start waiting now
+    grid_launch_dependents();
+    grid_dependency_wait();
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     auto sQc = [&](int c) { return base + kTileBytes * (uint32_t)c; };
     auto sKs = [&](int s) { return base + kTileBytes * (uint32_t)(kCrMaxChunks + s); };
@@ -1192,6 +1209,28 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
     if (warp == kCrMmaWarp) tmem_dealloc(tmem, kCrTmemCols);
 }
 
+// A launch with programmatic stream serialisation (the grid may start before the one it follows
+// has completed; it waits for that grid itself).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned threads, uint32_t smem, cudaStream_t stream,
+               Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ACACHE_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 // pdl: launched with programmatic stream serialisation after a grid that releases it early --
 // a store (store-then-attend; prm.early_wait orders the pool reads after it) or the attention
 // of another layer (chained layers; prm.early_wait = 0).
@@ -1294,7 +1333,7 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
 int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                            const void* k_req, const void* v_req, const void* k_aff,
                            const void* v_aff, void* out, float* stat_m, float* stat_l,
-                           int32_t* dev_status, cudaStream_t stream) {
+                           int32_t* dev_status, cudaStream_t stream, bool chained) {
     (void)l;   // key order inside a row does not change the softmax: affix tiles, then own tiles
     const int P = T_len - L;
     AttnParams prm{};
@@ -1311,7 +1350,11 @@ int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, co
     prm.stat_m = stat_m;
     prm.stat_l = stat_l;
     prm.dev_status = dev_status;
-    prm.early_wait = 1;
+    // chained: the probe of a later layer of one call, launched behind the previous layer's
+    // head sum with programmatic dependent launch; it starts while the previous layer's mass
+    // and head-sum grids finish, reads only its own layer's inputs (complete before the call's
+    // first grid) and waits for them before it writes its output and row statistics.
+    prm.early_wait = 2;
     prm.n_rows = P;
     prm.Hq = a.hq;
     prm.Hkv = a.hkv;
@@ -1320,7 +1363,7 @@ int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, co
     prm.P = P;
     prm.scale_log2 = a.scale * kLog2e;
     prm.budget = wait_budget();
-    return launch_attn<kProbeKeys>(prm, B, stream);
+    return launch_attn<kProbeKeys>(prm, B, stream, chained);
 }
 
 int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int32_t* masked_rows,
@@ -1370,16 +1413,14 @@ int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int
             (void)cudaGetLastError();
             return ACACHE_ERR_CUDA;
         }
-        tc_colsum_rows_kernel<<<(unsigned)ctas_r, kCrThreads, kCrSmemBytes, stream>>>(prm, per);
-        return launch_status();
+        return launch_pdl(tc_colsum_rows_kernel, (unsigned)ctas_r, kCrThreads, kCrSmemBytes, stream, prm, per);
     }
     if (cudaFuncSetAttribute(tc_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kCsSmemBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
     }
-    tc_colsum_kernel<<<(unsigned)ctas, kCsThreads, kCsSmemBytes, stream>>>(prm);
-    return launch_status();
+    return launch_pdl(tc_colsum_kernel, (unsigned)ctas, kCsThreads, kCsSmemBytes, stream, prm);
 }
 
 }  // namespace acache

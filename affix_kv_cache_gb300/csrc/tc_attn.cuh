@@ -42,7 +42,7 @@ int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q,
 int launch_tc_probe_pass_a(const AttnArgs& a, int B, int T_len, int l, int L, const void* q,
                            const void* k_req, const void* v_req, const void* k_aff,
                            const void* v_aff, void* out, float* stat_m, float* stat_l,
-                           int32_t* dev_status, cudaStream_t stream);
+                           int32_t* dev_status, cudaStream_t stream, bool chained = false);
 int launch_tc_probe_pass_b(const AttnArgs& a, int B, int T_len, int L, const int32_t* masked_rows,
                            int m, const void* q, const void* k_aff, const float* stat_m,
                            const float* stat_l, float* partial, int32_t* dev_status,

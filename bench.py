@@ -190,6 +190,10 @@ class Path:
         self.launches_per_step = w.layers * 3 + 2 + w.recompute_points * w.layers * 2
         torch.cuda.synchronize()
 
+    def probe_lists(self):
+        """Per-layer q, k_req, v_req, k_aff, v_aff lists of the probe inputs in use."""
+        return [[p[k] for p in self.probe] for k in ("q", "k_req", "v_req", "k_aff", "v_aff")]
+
     def step(self, ev=None):
         """One pass of the path.  `ev` (optional) collects CUDA events around phases."""
         ac, w, lay = self.ac, self.w, self.lay
@@ -198,11 +202,10 @@ class Path:
         if ev is not None:
             e0 = torch.cuda.Event(enable_timing=True)
             e0.record(s)
-        for n in range(w.layers):
-            p = self.probe[n]
-            ac.acache_probe_scores(self.desc, w.batch, w.T, w.l, w.L, self.masked, w.m, p["q"],
-                                   p["k_req"], p["v_req"], p["k_aff"], p["v_aff"], self.probe_out,
-                                   self.scores, self.ws, self.ws_bytes)
+        # the probe of every layer in one call (later layers' grids chained behind earlier ones)
+        ac.acache_probe_scores_layers(self.desc, w.batch, w.T, w.l, w.L, self.masked, w.m,
+                                      *self.probe_lists(), [self.probe_out] * w.layers, self.scores,
+                                      self.ws, self.ws_bytes)
         ac.acache_topk_anchors(self.scores, w.batch, w.L, w.K, self.anchors)
         if ev is not None:
             e1 = torch.cuda.Event(enable_timing=True)
@@ -562,12 +565,13 @@ def _per_launch_ms(fn, reps=5):
 
 
 def _launch_set(path):
-    """Per-launch times (ms) of one layer's probe, store and slot attention for the batch."""
+    """Per-launch times (ms) of one layer's probe (from one call over all the path's layers,
+    as a step makes it), store and slot attention for the batch."""
     ac, w, lay = path.ac, path.w, path.lay
-    p0, r0 = path.probe[0], path.rec[0]
-    probe = _per_launch_ms(lambda: ac.acache_probe_scores(
-        path.desc, w.batch, w.T, w.l, w.L, path.masked, w.m, p0["q"], p0["k_req"], p0["v_req"], p0["k_aff"],
-        p0["v_aff"], path.probe_out, path.scores, path.ws, path.ws_bytes))
+    r0 = path.rec[0]
+    probe = _per_launch_ms(lambda: ac.acache_probe_scores_layers(
+        path.desc, w.batch, w.T, w.l, w.L, path.masked, w.m, *path.probe_lists(),
+        [path.probe_out] * w.layers, path.scores, path.ws, path.ws_bytes)) / w.layers
     write = _per_launch_ms(lambda: ac.acache_write_slots(
         path.desc, w.batch, w.R, lay.private_slots, r0["k_new"], r0["v_new"], path.kc[0], path.vc[0],
         lay.num_slots, lay.private_begin))

@@ -135,6 +135,36 @@ ACACHE_API int acache_probe_scores(const acache_attn_desc* a, int batch, int seq
                         void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * (1)+(2) Anchor probe of every layer in one call.  Page: Sec. 3.2, Eq. 4-5 (the probe runs
+ * once per layer and the importance sums over layers).
+ *
+ * Computes exactly what acache_probe_scores(a, batch, ..., q[n], k_req[n], v_req[n],
+ * k_affix[n], v_affix[n], out ? out[n] : NULL, scores, workspace, ...) does for n = 0, 1,
+ * ..., layers-1 in that order on `stream`: the same kernels, the same accumulation order into
+ * `scores`, so the result is bit-identical to those per-layer calls.  The shapes, batch,
+ * masked rows, scores and workspace are shared by all layers; q, k_req, v_req, k_affix,
+ * v_affix and out are host arrays of `layers` device pointers each (out may be NULL, and so
+ * may an entry of it; k_affix/v_affix may be NULL when affix_len = 0).
+ *
+ * When nothing the call writes (any layer's out, scores, the workspace) overlaps any layer's
+ * q/k_req/v_req/k_affix/v_affix (checked on the host), the grids of layer n > 0 are chained
+ * behind layer n-1 with programmatic dependent launch (tensor-core path): layer n's probe
+ * forward starts on the SMs that layer n-1's mass and head-sum grids leave idle, reading its
+ * own layer's inputs at once and waiting for those grids before it writes anything.  Work
+ * enqueued on the stream after the call runs after all of it.  The inputs must therefore be
+ * complete before the call (as for any launch on the stream).  Otherwise -- or on the
+ * CUDA-core path -- the layers run one after the other.  Every argument of every layer is
+ * checked before anything is launched; errors as acache_probe_scores.
+ * ------------------------------------------------------------------------------- */
+ACACHE_API int acache_probe_scores_layers(const acache_attn_desc* a, int layers, int batch,
+                        int seq_len, int affix_begin, int affix_len, const int32_t* masked_rows,
+                        int num_masked, const void* const* q, const void* const* k_req,
+                        const void* const* v_req, const void* const* k_affix,
+                        const void* const* v_affix, void* const* out, float* scores,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Probe without a workspace.  The page has no counterpart: this entry point exists for
  * callers that cannot allocate device memory when they probe -- an engine that gives the
  * library only tensors it already owns (a memory budget split up at start-up, an allocator

@@ -214,6 +214,67 @@ def test_probe_accumulates_over_layers_and_is_deterministic():
     assert_scores_close(s1.cpu().numpy(), ref["scores"], "3-layer scores")
 
 
+@pytest.mark.parametrize("dtype,d,heads,feed", [("bf16", 128, (4, 2), False), ("bf16", 128, (4, 2), True),
+                                                ("f32", 64, (2, 2), False)])
+def test_probe_layers_matches_per_layer_calls(dtype, d, heads, feed):
+    """acache_probe_scores_layers is bit-identical to one acache_probe_scores call per layer.
+    feed: layer n's output buffer is layer n+1's query buffer, so the call must not chain
+    (the host's overlap check) and each layer reads what the previous one wrote."""
+    w = tiny(RAGGED["suffix"], hq=heads[0], hkv=heads[1], d=d, dtype=dtype, batch=2).replace(layers=4)
+    inps = [wl.probe_inputs(w, n) for n in range(w.layers)]
+    masked = dev(torch.tensor(w.masked_rows(), dtype=torch.int32).expand(w.batch, -1))
+    desc = desc_of(w)
+    need = ac.acache_probe_workspace_bytes(desc, w.batch, w.T, w.L, w.m)
+
+    def buffers():
+        qs = [dev(i["q"]) for i in inps]
+        outs = [torch.empty_like(q) for q in qs]
+        if feed:
+            outs = qs[1:] + [outs[-1]]
+        return qs, outs
+
+    ka = [dev(i["k_aff"]) for i in inps]
+    va = [dev(i["v_aff"]) for i in inps]
+    kr = [dev(i["k_req"]) for i in inps]
+    vr = [dev(i["v_req"]) for i in inps]
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s1 = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    st1 = status_tensor()
+    q1, o1 = buffers()
+    for n in range(w.layers):
+        ac.acache_probe_scores(desc, w.batch, w.T, w.l, w.L, masked, w.m, q1[n], kr[n], vr[n], ka[n], va[n],
+                               o1[n], s1, ws, dev_status=st1)
+    s2 = torch.zeros_like(s1)
+    st2 = status_tensor()
+    q2, o2 = buffers()
+    ac.acache_probe_scores_layers(desc, w.batch, w.T, w.l, w.L, masked, w.m, q2, kr, vr, ka, va, o2, s2,
+                                  ws, dev_status=st2)
+    torch.cuda.synchronize()
+    assert st1.item() == 0 and st2.item() == 0
+    assert torch.equal(s1, s2)
+    for a, b in zip(o1, o2):
+        assert torch.equal(a, b)
+    if not feed:
+        # again, without outputs, accumulating onto the first call's scores
+        ac.acache_probe_scores_layers(desc, w.batch, w.T, w.l, w.L, masked, w.m, q2, kr, vr, ka, va, None,
+                                      s2, ws, dev_status=st2)
+        for n in range(w.layers):
+            ac.acache_probe_scores(desc, w.batch, w.T, w.l, w.L, masked, w.m, q1[n], kr[n], vr[n], ka[n],
+                                   va[n], None, s1, ws, dev_status=st1)
+        torch.cuda.synchronize()
+        assert st1.item() == 0 and st2.item() == 0
+        assert torch.equal(s1, s2)
+        s2 = s2 / 2
+    if not feed:
+        ref = None
+        for n, inp in enumerate(inps):
+            ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
+                                     T=w.T, l=w.l, masked_rows=w.masked_rows(), scale=w.scale,
+                                     scores=None if ref is None else ref["scores"], want_out=n == w.layers - 1)
+        assert_scores_close(s2.cpu().numpy(), ref["scores"], "4-layer scores")
+        assert_out_close(o2[-1].float().cpu().numpy(), ref["out"], dtype, "last layer's probe output")
+
+
 def test_probe_bad_masked_row_is_skipped_and_flagged():
     w = tiny(SMALL, batch=2, d=64, dtype="f32")
     inp = wl.probe_inputs(w, 0)
