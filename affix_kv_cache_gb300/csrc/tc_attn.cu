@@ -1022,12 +1022,15 @@ __global__ void __launch_bounds__(kCrThreads, 1)
 tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta) {
     extern __shared__ uint8_t dsm[];
     __shared__ ColsumRowsCtl ctl;
-    // launched behind the probe forward (programmatic dependent launch): its row statistics are
-    // read below; the head sum after this grid may start waiting now
+    // Launched behind the probe forward (programmatic dependent launch), whose row statistics
+    // it reads: the producer warp loads the masked rows and the first key tiles (inputs of the
+    // call, complete before the forward started) and only then waits for the forward.  The
+    // head sum after this grid may start waiting at once.
     grid_launch_dependents();
-    grid_dependency_wait();
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
-    auto sQc = [&](int c) { return base + kTileBytes * (uint32_t)c; };
+    // Masked rows: 64-column half r of chunk c at sQ(c, r), so that the two chunks' halves are
+    // adjacent and one MMA operand of N = 256 rows covers both chunks.
+    auto sQ = [&](int c, int r) { return base + kTileBytes * (uint32_t)r + kRegion * (uint32_t)c; };
     auto sKs = [&](int s) { return base + kTileBytes * (uint32_t)(kCrMaxChunks + s); };
     const int n_jt = (p.L + kBN - 1) / kBN;
     const int n_grp = (n_jt + tiles_per_cta - 1) / tiles_per_cta;
@@ -1038,14 +1041,17 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
     const int jt0 = grp * tiles_per_cta;
     const int n_t = min(n_jt, jt0 + tiles_per_cta) - jt0;
     const int n_ch = (p.m + kBN - 1) / kBN;
-    if (n_t <= 0 || n_ch > kCrMaxChunks) return;
+    if (n_t <= 0 || n_ch > kCrMaxChunks) {
+        grid_dependency_wait();      // the grid still completes after the forward
+        return;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
     const long long budget = p.budget;
 
     if (threadIdx.x == 0) {
-        mbar_init(&ctl.q_full, 32);
+        mbar_init(&ctl.q_full, 33);   // the byte count's arrival + every producer lane's statistics
         for (int s = 0; s < kCrKStages; ++s) {
             mbar_init(&ctl.k_full[s], 1);
             mbar_init(&ctl.k_empty[s], 1);
@@ -1077,23 +1083,25 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_qbox);
         }
-        // The masked rows: every lane stores its rows' statistics, then arrives on q_full (lane
-        // 0 through the expect_tx that announces all chunks' bytes, before any load is issued).
-        int rows[kCrMaxChunks][4], r0[kCrMaxChunks];
+        // The masked rows (probe rows pr[c][u]; -1 = none or bad), then their loads: lane 0's
+        // expect_tx announces all chunks' bytes before any load is issued.
+        int rows[kCrMaxChunks][4], pr[kCrMaxChunks][4], r0[kCrMaxChunks];
         bool run[kCrMaxChunks];
 #pragma unroll
         for (int c = 0; c < kCrMaxChunks; ++c) {
             run[c] = false;
             r0[c] = 0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pr[c][u] = -1;
             if (c >= n_ch) continue;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int k = c * kBN + 4 * lane + u;
-                const int pr = k < p.m ? mrow[k] : -1;
-                const bool good = pr >= 0 && pr < p.P;
+                const int x = k < p.m ? mrow[k] : -1;
+                const bool good = x >= 0 && x < p.P;
                 if (k < p.m && !good) flag(dev_status, ACACHE_DEV_BAD_ROW);
-                rows[c][u] = good ? ((b * p.P + pr) * p.Hq + h) : oob_row;
-                ctl.st_off[c][4 * lane + u] = good ? sm_row[pr] + log2f(sl_row[pr]) : INFINITY;
+                rows[c][u] = good ? ((b * p.P + x) * p.Hq + h) : oob_row;
+                pr[c][u] = good ? x : -1;
             }
             // a chunk of consecutive probe rows (the generation positions) is two tiled box
             // loads; rows of the box past the masked set are skipped by their statistics
@@ -1114,22 +1122,41 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
             if (c >= n_ch) continue;
             if (run[c]) {
                 if (lane == 0) {
-                    tma_load_4d(sQc(c), &p.tm_qbox, 0, h, r0[c], b, &ctl.q_full);
-                    tma_load_4d(sQc(c) + kRegion, &p.tm_qbox, 64, h, r0[c], b, &ctl.q_full);
+                    tma_load_4d(sQ(c, 0), &p.tm_qbox, 0, h, r0[c], b, &ctl.q_full);
+                    tma_load_4d(sQ(c, 1), &p.tm_qbox, 64, h, r0[c], b, &ctl.q_full);
                 }
             } else {
                 const uint32_t o = (uint32_t)lane * 512u;
-                tma_gather4(sQc(c) + o, &p.tm_q, 0, rows[c][0], rows[c][1], rows[c][2], rows[c][3], &ctl.q_full);
-                tma_gather4(sQc(c) + kRegion + o, &p.tm_q, 64, rows[c][0], rows[c][1], rows[c][2], rows[c][3],
+                tma_gather4(sQ(c, 0) + o, &p.tm_q, 0, rows[c][0], rows[c][1], rows[c][2], rows[c][3], &ctl.q_full);
+                tma_gather4(sQ(c, 1) + o, &p.tm_q, 64, rows[c][0], rows[c][1], rows[c][2], rows[c][3],
                             &ctl.q_full);
             }
         }
-        if (lane != 0) mbar_arrive(&ctl.q_full);
-        // the run's affix key tiles, kCrKStages stages
-        for (int i = 0; i < n_t; ++i) {
+        // the first affix key tiles (every stage is free)
+        const int n_pre = min(n_t, kCrKStages);
+        if (lane == 0) {
+            for (int i = 0; i < n_pre; ++i) {
+                mbar_arrive_expect_tx(&ctl.k_full[i], kTileBytes);
+                tma_load_3d(sKs(i), &p.tm_kaff, 0, hk, (jt0 + i) * kBN, &ctl.k_full[i]);
+                tma_load_3d(sKs(i) + kRegion, &p.tm_kaff, 64, hk, (jt0 + i) * kBN, &ctl.k_full[i]);
+            }
+        }
+        // The row statistics are the forward's output: wait for that grid, then read them past
+        // L1.  Each probability is 2^(logit - off) with off = row maximum + log2(row sum).
+        grid_dependency_wait();
+#pragma unroll
+        for (int c = 0; c < kCrMaxChunks; ++c) {
+            if (c >= n_ch) continue;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                ctl.st_off[c][4 * lane + u] =
+                    pr[c][u] >= 0 ? __ldcg(sm_row + pr[c][u]) + log2f(__ldcg(sl_row + pr[c][u])) : INFINITY;
+        }
+        mbar_arrive(&ctl.q_full);
+        // the rest of the run's affix key tiles, kCrKStages stages
+        for (int i = n_pre; i < n_t; ++i) {
             const int s = i % kCrKStages;
-            if (i >= kCrKStages &&
-                !__all_sync(0xffffffffu,
+            if (!__all_sync(0xffffffffu,
                             wait_bar(&ctl.k_empty[s], ((i / kCrKStages) - 1) & 1, abort_flag, dev_status, budget)))
                 break;
             if (lane == 0) {
@@ -1142,7 +1169,9 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
         }
     } else if (warp == kCrMmaWarp) {
         if (lane == 0) {
-            const uint32_t id = idesc_bf16(kBN, kBN, false, false);
+            // one MMA per k-step covers every chunk: N = 128 or 256 masked rows (rows past m are
+            // zero-filled by their loads, so every column the consumers read is written)
+            const uint32_t id = idesc_bf16(kBN, kBN * n_ch, false, false);
             bool ok = wait_bar(&ctl.q_full, 0, abort_flag, dev_status, budget);
             for (int i = 0; ok && i < n_t; ++i) {
                 const int ks = i % kCrKStages, db = i & 1;     // key stage, D buffer
@@ -1150,13 +1179,11 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
                 if (ok && i >= 2) ok = wait_bar(&ctl.cons_done[db], ((i >> 1) - 1) & 1, abort_flag, dev_status, budget);
                 if (!ok) break;
                 tc_fence_after();
-                for (int c = 0; c < n_ch; ++c) {
 #pragma unroll
-                    for (int k = 0; k < kD / 16; ++k) {
-                        const uint32_t ko = (uint32_t)(k >> 2) * kRegion + (uint32_t)(k & 3) * 32u;
-                        umma_ss(tmem + (uint32_t)db * 256u + (uint32_t)c * kBN, sdesc_sw128(sKs(ks) + ko, 16, 1024),
-                                sdesc_sw128(sQc(c) + ko, 16, 1024), id, k > 0);
-                    }
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t kcol = (uint32_t)(k & 3) * 32u;     // 16 columns within a half
+                    umma_ss(tmem + (uint32_t)db * 256u, sdesc_sw128(sKs(ks) + (uint32_t)(k >> 2) * kRegion + kcol, 16, 1024),
+                            sdesc_sw128(sQ(0, k >> 2) + kcol, 16, 1024), id, k > 0);
                 }
                 umma_commit(&ctl.d_full[db]);
                 umma_commit(&ctl.k_empty[ks]);
