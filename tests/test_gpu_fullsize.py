@@ -224,3 +224,44 @@ def test_fullsize_chained_layers_repeat():
         assert st.item() == 0, f"device status {st.item()} in run {r}"
         for n in range(layers):
             assert torch.equal(out[n], ref[n]), f"run {r}, layer {n}"
+
+
+@pytest.mark.parametrize("w", FULL, ids=IDS)
+def test_fullsize_probe_layers_chained(w):
+    """The probe of four layers in one call (each layer's forward chained behind the previous
+    layer's head sum, starting while the previous layer's mass pass runs), repeated: no device
+    error, and scores and outputs equal the per-layer calls bit for bit every time.  The first
+    request's scores are checked against the oracle's four-layer sum."""
+    layers, reps = 4, 3
+    d = desc_of(w)
+    inps = [wl.probe_inputs(w, n, device="cuda") for n in range(layers)]
+    lists = [[i[k] for i in inps] for k in ("q", "k_req", "v_req", "k_aff", "v_aff")]
+    masked = torch.tensor(w.masked_rows(), dtype=torch.int32, device="cuda").expand(w.batch, -1).contiguous()
+    ws = torch.empty(ac.acache_probe_workspace_bytes(d, w.batch, w.T, w.L, w.m), dtype=torch.uint8,
+                     device="cuda")
+    st = status_tensor()
+    ref_s = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    ref_o = [torch.empty_like(i["q"]) for i in inps]
+    for n, i in enumerate(inps):
+        ac.acache_probe_scores(d, w.batch, w.T, w.l, w.L, masked, w.m, i["q"], i["k_req"], i["v_req"],
+                               i["k_aff"], i["v_aff"], ref_o[n], ref_s, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    out = [torch.empty_like(o) for o in ref_o]
+    for r in range(reps):
+        s = torch.zeros_like(ref_s)
+        for o in out:
+            o.zero_()
+        ac.acache_probe_scores_layers(d, w.batch, w.T, w.l, w.L, masked, w.m, *lists, out, s, ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0, f"device status {st.item()} in run {r}"
+        assert torch.equal(s, ref_s), f"scores, run {r}"
+        for n in range(layers):
+            assert torch.equal(out[n], ref_o[n]), f"run {r}, layer {n}"
+    ref = None
+    for i in inps:
+        cpu = {k: v[:1].cpu() if k in ("q", "k_req", "v_req") else v.cpu() for k, v in i.items()}
+        ref = oracle.probe_layer(cpu["q"], cpu["k_req"], cpu["v_req"], cpu["k_aff"], cpu["v_aff"], T=w.T, l=w.l,
+                                 masked_rows=w.masked_rows(), scale=w.scale, want_out=False,
+                                 scores=None if ref is None else ref["scores"])
+    assert_scores_close(ref_s[:1].cpu().numpy(), ref["scores"], f"{w.name} four-layer scores")
