@@ -9,7 +9,8 @@ from ._lib import (AcacheError, AttnDesc, attn_desc, acache_build_slot_maps,  # 
                    acache_gather_slots, acache_kv_deviation_scores, acache_probe_scores,
                    acache_probe_scores_layers, acache_probe_scores_noalloc,
                    acache_probe_workspace_bytes,
-                   acache_slot_attention, acache_slot_attention_dropna, acache_slot_attention_varlen,
+                   acache_slot_attention, acache_slot_attention_dropna, acache_slot_attention_path,
+                   acache_slot_attention_varlen,
                    acache_rerotate_keys, acache_store_attend, acache_store_attend_layers, acache_topk_anchors, Pool,
                    acache_wait_budget, acache_write_slots, lib,
                    status_string, version)

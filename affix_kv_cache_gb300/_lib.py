@@ -24,6 +24,9 @@ ACACHE_ERR_WORKSPACE = -4
 ACACHE_ERR_TIMEOUT = -5
 ACACHE_F32 = 0
 ACACHE_BF16 = 1
+ACACHE_PATH_RECOMPUTE = 0
+ACACHE_PATH_BLOCK_DECODE = 1
+ACACHE_PATH_CUDA_CORES = 2
 SLOT_NONE = -1
 DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
 DEV_BAD_LENGTH = 64
@@ -32,6 +35,7 @@ EXPORTS = ("acache_status_string", "acache_version", "acache_wait_budget", "acac
            "acache_probe_scores", "acache_probe_scores_layers", "acache_probe_scores_noalloc", "acache_topk_anchors", "acache_build_slot_maps",
            "acache_write_slots", "acache_slot_attention", "acache_gather_slots",
            "acache_kv_deviation_scores", "acache_slot_attention_dropna", "acache_slot_attention_varlen",
+           "acache_slot_attention_path",
            "acache_store_attend", "acache_store_attend_layers", "acache_rerotate_keys", "acache_pool_create",
            "acache_pool_destroy",
            "acache_pool_register_affix", "acache_pool_release_affix", "acache_pool_alloc_private",
@@ -83,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "acache_build_slot_maps": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
             "acache_write_slots": (I, [D, I, I, P, P, P, P, P, I64, I64, P, P]),
             "acache_slot_attention": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
+            "acache_slot_attention_path": (I, [D, I, I, I]),
             "acache_gather_slots": (I, [D, I, I, P, P, P, I64, P, P, P, P]),
             "acache_kv_deviation_scores": (I, [D, I, I, P, P, P, P, P, P]),
             "acache_slot_attention_dropna": (I, [D, I, I, P, I, P, P, P, I64, P, P, P]),
@@ -246,6 +251,13 @@ def acache_slot_attention_dropna(desc, batch, n_q, q, seq_len, read_slot, k_cach
                                             _p(read_slot), _p(k_cache), _p(v_cache), num_slots,
                                             _p(out), _p(dev_status), _stream(stream))
     return _check("acache_slot_attention_dropna", st) if check else st
+
+
+def acache_slot_attention_path(desc, batch, n_q, seq_len) -> int:
+    """The kernel acache_slot_attention runs for this geometry: ACACHE_PATH_RECOMPUTE,
+    ACACHE_PATH_BLOCK_DECODE or ACACHE_PATH_CUDA_CORES (see include/acache.h)."""
+    st = int(lib().acache_slot_attention_path(ctypes.byref(desc), batch, n_q, seq_len))
+    return _check("acache_slot_attention_path", st) if st < 0 else st
 
 
 def acache_slot_attention_varlen(desc, batch, q_start, max_q_rows, total_q_rows, q, kv_start,

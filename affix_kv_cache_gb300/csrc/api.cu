@@ -133,7 +133,7 @@ int slot_attention(const acache_attn_desc* desc, int batch, int n_q, const void*
     if (tc_supported(a)) {
         // few query rows per KV head (the block-decode step): the kernel that packs a GQA
         // group's heads into one K/V stream and splits the keys over a cluster
-        if (tc_decode_preferred(a, n_q))
+        if (tc_decode_preferred(a, batch, n_q, seq_len))
             return launch_tc_decode_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
                                               num_slots, out, dev_status, stream, drop_none, after_store);
         return launch_tc_slot_attention(a, batch, n_q, q, seq_len, read_slot, k_cache, v_cache,
@@ -300,6 +300,14 @@ int acache_probe_scores_layers(const acache_attn_desc* desc, int layers, int bat
     return ACACHE_OK;
 }
 
+int acache_slot_attention_path(const acache_attn_desc* desc, int batch, int n_q, int seq_len) {
+    AttnArgs a;
+    if (int rc = check_desc(desc, &a)) return rc;
+    if (batch < 0 || n_q < 0 || seq_len < 0) return ACACHE_ERR_INVALID_ARG;
+    if (!tc_supported(a)) return ACACHE_PATH_CUDA_CORES;
+    return tc_decode_preferred(a, batch, n_q, seq_len) ? ACACHE_PATH_BLOCK_DECODE : ACACHE_PATH_RECOMPUTE;
+}
+
 int acache_topk_anchors(const float* scores, int batch, int affix_len, int k, int32_t* anchors,
                         int32_t* dev_status, void* stream) {
     if (batch < 0 || affix_len < 0 || k < 0 || k > affix_len) return ACACHE_ERR_INVALID_ARG;
@@ -436,7 +444,7 @@ int acache_store_attend_layers(const acache_attn_desc* desc, int layers, int bat
                     if (x.lo < x.hi && y.lo < y.hi && x.lo < y.hi && y.lo < x.hi) disjoint = false;
         }
     }
-    const bool chain = disjoint && layers > 1 && (!attend || (tc_supported(a) && !tc_decode_preferred(a, n_q)));
+    const bool chain = disjoint && layers > 1 && (!attend || (tc_supported(a) && !tc_decode_preferred(a, batch, n_q, seq_len)));
     if (!chain) {
         for (int l = 0; l < layers; ++l)
             if (int rc = acache_store_attend(desc, batch, rows, write_slot, store ? k_new[l] : nullptr,

@@ -33,8 +33,9 @@ int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_s
                                     int64_t num_slots, void* out, int32_t* dev_status,
                                     cudaStream_t stream, bool drop_none);
 // Block-decode form of the read-slot attention (few query rows per KV head): true when it
-// streams fewer K/V tiles than the recompute-point kernel for this geometry.
-bool tc_decode_preferred(const AttnArgs& a, int n_q);
+// streams fewer K/V tiles than the recompute-point kernel for this geometry, or as many and
+// the streams would leave most SMs idle (its cluster split of the keys fills them).
+bool tc_decode_preferred(const AttnArgs& a, int B, int n_q, int T_len);
 int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                                const int32_t* read_slot, const void* k_cache, const void* v_cache,
                                int64_t num_slots, void* out, int32_t* dev_status, cudaStream_t stream,

@@ -618,7 +618,7 @@ int launch_rep(const DecParams& prm, int64_t ctas, cudaStream_t stream, bool pdl
 
 }  // namespace
 
-bool tc_decode_preferred(const AttnArgs& a, int n_q) {
+bool tc_decode_preferred(const AttnArgs& a, int B, int n_q, int T_len) {
     if (a.hkv <= 0 || a.hq % a.hkv) return false;
     const int g = a.hq / a.hkv;
     const int64_t rg = (int64_t)n_q * g;
@@ -628,7 +628,14 @@ bool tc_decode_preferred(const AttnArgs& a, int n_q) {
     const int64_t qpb = std::min(n_q, G / g);
     const int64_t streams_dec = (n_q + qpb - 1) / qpb;            // K/V streams per KV head
     const int64_t streams_main = (int64_t)g * ((n_q + 255) / 256);
-    return streams_dec < streams_main || (streams_dec == streams_main && n_q <= 128);
+    if (streams_dec != streams_main) return streams_dec < streams_main;
+    // As many K/V streams either way (one query head per KV head): the recompute kernel's
+    // lone-tile CTA, whose two chains split the keys, runs a stream slightly faster (measured
+    // at 32 queries: 23.4 against 24.9 us with 4 requests, 249 against 267 us with 16); the
+    // block-decode kernel still wins when the streams would leave most SMs idle and its
+    // cluster split of the keys fills them (a request or two).
+    (void)T_len;
+    return n_q <= 128 && (int64_t)B * a.hkv * streams_dec * 2 <= (int64_t)sm_count();
 }
 
 int launch_tc_decode_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,

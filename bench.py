@@ -375,6 +375,12 @@ class Decode:
         t_fused = replay_ms(graphs["fused"]) if graphs.get("fused") is not None else None
         attn_ms, write_ms = t_attn / per, t_write / per
         achieved = self.unique_bytes / (attn_ms / 1e3) / 1e9
+        # the kernel the library picks for this geometry (one query head per KV head and enough
+        # requests: the recompute kernel, whose lone query tile splits the keys over two chains)
+        path = self.p.ac.acache_slot_attention_path(self.p.desc, w.batch, self.n, w.T)
+        kernel, src = {self.p.ac._lib.ACACHE_PATH_RECOMPUTE: ("tc_attn_kernel (split keys)", "tc_attn.cu"),
+                       self.p.ac._lib.ACACHE_PATH_BLOCK_DECODE: ("tc_decode_kernel", "tc_decode.cu")}.get(
+                           path, ("simt", None))
         return {
             "workload": w.name, "block": self.n, "layers": w.layers, "replays": reps,
             "timing": f"CUDA graph replay, {per} launches of each kind per replay",
@@ -383,12 +389,12 @@ class Decode:
             "attn_tflops": 4.0 * self.n * w.T * w.d * w.hq * w.batch / (attn_ms / 1e3) / 1e12,
             "logical_gather_gbs": self.logical_bytes / (attn_ms / 1e3) / 1e9,
             "write_gbs": self.write_bytes / (write_ms / 1e3) / 1e9,
-            "roofline": {"bound": "hbm", "kernel": "decode_slot_attention", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "peak_source": f"{peaks['source']} HBM copy",
                          "bytes_per_launch": self.unique_bytes,
-                         "traffic": profiled_traffic(["affix_kv_cache_gb300/csrc/tc_decode.cu"], w.name,
-                                                     "decode_slot_attention_llada8b_prefix.md")},
+                         "traffic": None if src is None else profiled_traffic(
+                             [f"affix_kv_cache_gb300/csrc/{src}"], w.name, "decode_slot_attention_llada8b_prefix.md")},
         }
 
 

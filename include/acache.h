@@ -283,6 +283,17 @@ ACACHE_API int acache_slot_attention(const acache_attn_desc* a, int batch, int n
                           const void* v_cache, int64_t num_slots, void* out,
                           int32_t* dev_status, void* stream);
 
+/* Which kernel acache_slot_attention (and the attention of acache_store_attend) runs for a
+ * geometry (host only, no GPU call): ACACHE_PATH_RECOMPUTE -- the tcgen05 kernel of two
+ * 128-row query tiles per CTA (a lone tile splits its keys between two chains);
+ * ACACHE_PATH_BLOCK_DECODE -- the tcgen05 kernel for few query rows per KV head, chosen when
+ * it streams fewer K/V tiles (a GQA group's heads share one stream) or, with as many, when
+ * the streams would leave most SMs idle and its cluster split of the keys fills them;
+ * ACACHE_PATH_CUDA_CORES --
+ * float32 or bf16 at d = 64.  Returns a negative status for invalid arguments. */
+enum { ACACHE_PATH_RECOMPUTE = 0, ACACHE_PATH_BLOCK_DECODE = 1, ACACHE_PATH_CUDA_CORES = 2 };
+ACACHE_API int acache_slot_attention_path(const acache_attn_desc* a, int batch, int n_q, int seq_len);
+
 /* ---------------------------------------------------------------------------------
  * (4a') Store-then-attend over the layers of one recompute point.  Page: Sec. 4.3 and
  * App. C.1 (each layer stores its recomputed rows, then attends through the read-slot map).

@@ -122,3 +122,17 @@ def test_binding_raises_on_error():
     with pytest.raises(ac.AcacheError) as e:
         ac.acache_topk_anchors(None, 1, 10, 3, None)
     assert e.value.status == _lib.ACACHE_ERR_INVALID_ARG
+
+
+def test_slot_attention_path_choice():
+    """Host-only: which kernel the read-slot attention picks for a geometry."""
+    path = lambda hq, hkv, B, n_q, T, dt="bf16", d=128: ac.acache_slot_attention_path(  # noqa: E731
+        ac.attn_desc(hq, hkv, d, d ** -0.5, dt), B, n_q, T)
+    assert path(32, 32, 4, 589, 1408) == _lib.ACACHE_PATH_RECOMPUTE      # a recompute point
+    assert path(32, 32, 4, 32, 1408) == _lib.ACACHE_PATH_RECOMPUTE       # decode, 128 streams
+    assert path(32, 32, 1, 32, 1408) == _lib.ACACHE_PATH_BLOCK_DECODE    # decode, 32 streams
+    assert path(28, 4, 16, 32, 2624) == _lib.ACACHE_PATH_BLOCK_DECODE    # GQA group shares a stream
+    assert path(2, 2, 1, 32, 100, "f32", 64) == _lib.ACACHE_PATH_CUDA_CORES
+    assert path(8, 8, 1, 32, 100, "bf16", 64) == _lib.ACACHE_PATH_CUDA_CORES
+    with pytest.raises(ac.AcacheError):
+        path(3, 2, 1, 32, 100)                                            # Hq % Hkv != 0
