@@ -53,6 +53,9 @@ def parse():
                     help="profiling only: run this many layers instead of the workload's")
     ap.add_argument("--points", type=int, default=0,
                     help="profiling only: recompute points per step instead of the workload's")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="profiling only: one step to build the maps, then the block-decode "
+                         "measurement alone (its JSON record)")
     return ap.parse_args()
 
 
@@ -773,6 +776,12 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     path = Path(w, dev, seed_offset=rank)
+    if args.decode_only:
+        path.step()
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps(Decode(path).measure(2, 2, measured_peaks())))
+        return
     for _ in range(max(args.warmup, 3)):
         path.step()
     torch.cuda.synchronize()
