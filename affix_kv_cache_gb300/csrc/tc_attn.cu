@@ -1013,6 +1013,7 @@ struct ColsumRowsCtl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    int unlanded;                     // abort path: a load issued before the abort may not have landed
     float st_off[kCrMaxChunks][kBN];  // per masked row: row maximum (log2 domain) + log2(row
                                       // sum), so its probabilities are 2^(logit - off); +inf = skip
     float xsum[2][kBN];               // the second consumer warpgroup's sums, by tile parity
@@ -1062,6 +1063,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
         }
         mbar_init(&ctl.drain, 1);
         ctl.abort = 0;
+        ctl.unlanded = 0;
         fence_mbar_init();
     }
     if (warp == kCrMmaWarp) {
@@ -1154,6 +1156,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
         }
         mbar_arrive(&ctl.q_full);
         // the rest of the run's affix key tiles, kCrKStages stages
+        int armed = n_pre - 1;                               // last key tile loaded
         for (int i = n_pre; i < n_t; ++i) {
             const int s = i % kCrKStages;
             if (!__all_sync(0xffffffffu,
@@ -1165,7 +1168,17 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
                 tma_load_3d(sKs(s), &p.tm_kaff, 0, hk, j0, &ctl.k_full[s]);
                 tma_load_3d(sKs(s) + kRegion, &p.tm_kaff, 64, hk, j0, &ctl.k_full[s]);
             }
+            armed = i;
             __syncwarp();
+        }
+        // Abort: every load this warp issued lands before the CTA exits.  Only the last tile
+        // of each stage can still be in flight; wait, bounded, for those phases and the masked
+        // rows, else hold the CTA for a fixed time.
+        if (*abort_flag && lane == 0) {
+            bool landed = mbar_wait(&ctl.q_full, 0, kLandBudget);
+            for (int e = max(0, armed - kCrKStages + 1); e <= armed; ++e)
+                landed = mbar_wait(&ctl.k_full[e % kCrKStages], (uint32_t)(e / kCrKStages) & 1u, kLandBudget) && landed;
+            if (!landed) ctl.unlanded = 1;
         }
     } else if (warp == kCrMmaWarp) {
         if (lane == 0) {
@@ -1232,7 +1245,7 @@ tc_colsum_rows_kernel(const __grid_constant__ ColsumParams p, int tiles_per_cta)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    settle_after_abort(*abort_flag != 0);
+    if (*abort_flag) settle_after_abort(ctl.unlanded != 0);
     if (warp == kCrMmaWarp) tmem_dealloc(tmem, kCrTmemCols);
 }
 

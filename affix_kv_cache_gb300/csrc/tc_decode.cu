@@ -69,6 +69,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColO = 256, kColP0 = 384;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr long long kDrainBudget = 1LL << 31;   // cycles: MMAs issued before an abort
+constexpr long long kLandBudget = 1LL << 21;    // cycles (~1 ms): TMA loads issued before an abort
 
 struct DecParams {
     CUtensorMap tm_q;     // 4-D [B][n_q][Hq][d], box {64, g, qpb, 1}
@@ -96,6 +97,7 @@ struct DecCtl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    int unlanded;         // abort path: some TMA load issued before the abort may not have landed
     float part_m[kBM];    // per TMEM lane: row maximum (log2 units) of the replica's keys
     float part_l[kBM];    // per TMEM lane: row sum
 };
@@ -163,6 +165,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
         mbar_init(&ctl.pv_done, 1);
         mbar_init(&ctl.drain, 1);
         ctl.abort = 0;
+        ctl.unlanded = 0;
         fence_mbar_init();
     }
     // Q rows the TMA does not write (past the block's packed rows) must be finite: zero the
@@ -227,6 +230,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
             resolve(0, next);
             // store-then-attend: wait for the preceding store grid before reading the pool
             grid_dependency_wait();
+            int armed = -1;                               // last entry this warp loaded into
             for (int j = 0; j < n_kv; ++j) {
                 const int s = j % kStages;
                 int rows[4] = {next[0], next[1], next[2], next[3]};
@@ -235,10 +239,21 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
                     !__all_sync(0xffffffffu, wait_bar(&empty[s], ((j / kStages) - 1) & 1, abort_flag, dev_status, budget)))
                     break;
                 if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
+                armed = j;
                 __syncwarp();
                 if (gathers)
                     tma_gather4((is_v ? sV(s) : sK(s)) + (uint32_t)half * kRegion + (uint32_t)gi * 512u, tm,
                                 half * 64, rows[0], rows[1], rows[2], rows[3], &full[s]);
+            }
+            // Abort: the loads this warp issued land before the CTA exits.  Only the last entry
+            // of each stage can still have loads in flight, so wait, bounded, for those phases
+            // (and for the query rows); a phase that another warp of the ring never loaded
+            // into cannot complete, and then the CTA holds for a fixed time instead.
+            if (*abort_flag) {
+                bool landed = is_v || pi != 0 || mbar_wait(&ctl.q_full, 0, kLandBudget);
+                for (int e = max(0, armed - kStages + 1); e <= armed; ++e)
+                    landed = mbar_wait(&full[e % kStages], (uint32_t)(e / kStages) & 1u, kLandBudget) && landed;
+                if (!__all_sync(0xffffffffu, landed) && lane == 0) ctl.unlanded = 1;
             }
         } else {
             // ------------------------------------------------------------------ MMA issuer
@@ -461,7 +476,7 @@ tc_decode_kernel(const __grid_constant__ DecParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    settle_after_abort(*abort_flag != 0);
+    if (*abort_flag) settle_after_abort(ctl.unlanded != 0);
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
     if (REP == 1 && cs == 1) return;
 
