@@ -209,6 +209,10 @@ class Path:
         ac.acache_probe_scores_layers(self.desc, w.batch, w.T, w.l, w.L, self.masked, w.m,
                                       *self.probe_lists(), [self.probe_out] * w.layers, self.scores,
                                       self.ws, self.ws_bytes)
+        if ev is not None:
+            ep = torch.cuda.Event(enable_timing=True)
+            ep.record(s)
+            ev["probe"].append((e0, ep))
         ac.acache_topk_anchors(self.scores, w.batch, w.L, w.K, self.anchors)
         if ev is not None:
             e1 = torch.cuda.Event(enable_timing=True)
@@ -794,7 +798,7 @@ def main():
     def max_over_ranks(x):
         return reduce_max(x, dev)
 
-    ev = {"select": []}
+    ev = {"select": [], "probe": []}
     clocks = ClockSampler(os.path.join(tempfile.gettempdir(), f"acache_clocks_{os.getpid()}_r{rank}.csv"))
     barrier()
     torch.cuda.synchronize()
@@ -811,8 +815,10 @@ def main():
     tflops = step_flops(w) * args.steps * world / (ms / 1e3) / 1e12
     slot_ms, slot_alone_ms = slot_launch_times(path)
     select_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["select"])
+    probe_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["probe"])
     scored_tok_s = w.batch * w.L / (select_ms / 1e3)
     peaks = measured_peaks()
+    probe_achieved = probe_flops(w) / (probe_ms / 1e3) / 1e12
     slot_achieved = slot_flops_per_launch(w) / (slot_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     traffic = profiled_traffic(["affix_kv_cache_gb300/csrc/tc_attn.cu"], w.name)
@@ -886,6 +892,14 @@ def main():
                        "l2": f"inputs larger than L2: {gb_touched / 1e9:.1f} GB touched per step"},
             "anchor_scored_tokens_per_s": scored_tok_s,
             "select_ms": select_ms,
+            "probe_ms": probe_ms,
+            "probe_roofline": {"bound": "tensor", "kernel": "probe (forward + mass + head sum, all layers, "
+                                                           "one chained call)",
+                               "achieved": probe_achieved, "peak": peaks["bf16_tflops_sustained"],
+                               "unit": "TFLOP/s", "frac": probe_achieved / peaks["bf16_tflops_sustained"],
+                               "flops": "the forward's 4·P·T·d per row-head-layer only (the mass pass's "
+                                        "2·m·L·d recompute not counted)",
+                               "peak_source": f"{peaks['source']} bf16 sustained"},
             "slot_attn_ms_per_launch": slot_ms,
             "slot_attn_timing": "per launch within one call over all layers (launches chained); "
                                 "slot_attn_ms_per_launch_alone: one launch at a time",
