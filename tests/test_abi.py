@@ -136,3 +136,21 @@ def test_slot_attention_path_choice():
     assert path(8, 8, 1, 32, 100, "bf16", 64) == _lib.ACACHE_PATH_CUDA_CORES
     with pytest.raises(ac.AcacheError):
         path(3, 2, 1, 32, 100)                                            # Hq % Hkv != 0
+
+
+def test_probe_layers_host_validation():
+    """Host-only checks of acache_probe_scores_layers: nothing is launched on bad input."""
+    L = ac.lib()
+    d = desc(hq=4, hkv=2)
+    E, W = _lib.ACACHE_ERR_INVALID_ARG, _lib.ACACHE_ERR_WORKSPACE
+    arr = (ctypes.c_void_p * 3)(BOGUS, BOGUS, BOGUS)
+    bad = (ctypes.c_void_p * 3)(BOGUS, BOGUS + 8, BOGUS)        # layer 1's pointer misaligned
+    nul = (ctypes.c_void_p * 3)(BOGUS, None, BOGUS)             # layer 1's pointer missing
+    args = lambda q, n=3, ws=1 << 30: (ctypes.byref(d), n, 2, 64, 0, 32, BOGUS, 16, q, arr, arr, arr, arr,  # noqa: E731
+                                       None, BOGUS, BOGUS, ws, None, None)
+    assert L.acache_probe_scores_layers(*args(arr, n=-1)) == E
+    assert L.acache_probe_scores_layers(*args(arr, n=0)) == _lib.ACACHE_OK     # nothing to do
+    assert L.acache_probe_scores_layers(*args(None)) == E                      # no query array
+    assert L.acache_probe_scores_layers(*args(bad)) == E
+    assert L.acache_probe_scores_layers(*args(nul)) == E
+    assert L.acache_probe_scores_layers(*args(arr, ws=16)) == W
