@@ -112,7 +112,8 @@ ACACHE_API int64_t acache_wait_budget(int64_t cycles);
  * (value rows likewise).  Softmax runs over the full row.  Then, for every initially
  * masked row k and affix offset j:  scores[b][j] += softmax_row_k[l + j], summed over
  * heads in ascending order.  Call layers 0..N-1 in order on one stream, after zeroing
- * `scores`; that fixes the accumulation order, so results are bit-reproducible.
+ * `scores`; that fixes the accumulation order, so results are bit-reproducible
+ * (acache_probe_scores_layers makes the same calls for every layer at once).
  *
  *   q            [B][P][Hq][d]   probe-row queries, rows in ascending logical order
  *   k_req, v_req [B][P][Hkv][d]  the request's own K/V rows (same order)
