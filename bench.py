@@ -121,9 +121,20 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+        # nvidia-smi takes a moment to start: wait (up to 3 s) for its first sample, then count
+        # only the samples taken from here on, inside the timed region
+        self.skip = 0
+        if self.proc is not None:
+            t_end = time.time() + 3.0
+            while time.time() < t_end and self.proc.poll() is None:
+                self.f.flush()
+                if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.02)
+            self.skip = sum(1 for _ in open(self.path)) if os.path.exists(self.path) else 0
         return self
 
     def __exit__(self, *a):
@@ -140,7 +151,9 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for n_line, line in enumerate(open(self.path)):
+            if n_line < self.skip:
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9 or not parts[0].isdigit() or int(parts[0]) != device_index:
                 continue
