@@ -513,3 +513,49 @@ def test_tiny_prefix_f32_pipeline():
     assert np.array_equal(wp.cpu().numpy(), wp_ref) and np.array_equal(rs.cpu().numpy(), rs_ref)
     assert torch.equal(kc.cpu(), kc_ref) and torch.equal(vc.cpu(), vc_ref)
     assert_out_close(out.cpu().numpy(), o_ref, "f32", "slot attention")
+
+
+@pytest.mark.parametrize("case", ["no_masked_rows", "no_affix", "one_layer"])
+def test_probe_layers_edge_cases(case):
+    """The chained probe of several layers at its edges: no masked row (every score stays 0), no
+    affix (only the request's own keys: no mass, no head sum; the forwards chain directly) and a
+    single layer -- each equal to the per-layer calls bit for bit and to the oracle."""
+    segs = {"no_masked_rows": [(wl.SEG_AFFIX, 300), (wl.SEG_REQ, 200)],
+            "no_affix": [(wl.SEG_REQ, 150), (wl.SEG_MASK, 150)],
+            "one_layer": [(wl.SEG_REQ, 60), (wl.SEG_AFFIX, 300), (wl.SEG_MASK, 140)]}[case]
+    w = tiny(segs, batch=2).replace(layers=1 if case == "one_layer" else 3)
+    inps = [wl.probe_inputs(w, n) for n in range(w.layers)]
+    desc = desc_of(w)
+    masked = dev(torch.tensor(w.masked_rows(), dtype=torch.int32).reshape(1, -1).expand(w.batch, -1).contiguous())
+    ws = torch.empty(max(1, ac.acache_probe_workspace_bytes(desc, w.batch, w.T, w.L, w.m)), dtype=torch.uint8,
+                     device="cuda")
+    lists = [[dev(i[k]) if i[k].numel() else None for i in inps] for k in ("q", "k_req", "v_req", "k_aff", "v_aff")]
+    s1 = torch.zeros((w.batch, max(w.L, 1)), dtype=torch.float32, device="cuda")
+    s2 = torch.zeros_like(s1)
+    o1 = [torch.empty_like(q) for q in lists[0]]
+    o2 = [torch.empty_like(q) for q in lists[0]]
+    st = status_tensor()
+    sc1 = s1 if w.L else None
+    sc2 = s2 if w.L else None
+    for n in range(w.layers):
+        ac.acache_probe_scores(desc, w.batch, w.T, w.l, w.L, masked, w.m, lists[0][n], lists[1][n], lists[2][n],
+                               lists[3][n], lists[4][n], o1[n], sc1, ws, dev_status=st)
+    ac.acache_probe_scores_layers(desc, w.batch, w.T, w.l, w.L, masked, w.m,
+                                  *[lst if any(x is not None for x in lst) else None for lst in lists],
+                                  o2, sc2, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(s1, s2)
+    for a, b in zip(o1, o2):
+        assert torch.equal(a, b)
+    ref = None
+    for n, inp in enumerate(inps):
+        ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"], T=w.T, l=w.l,
+                                 masked_rows=w.masked_rows(), scale=w.scale,
+                                 scores=None if ref is None else ref["scores"])
+        assert_out_close(o2[n].float().cpu().numpy(), ref["out"], "bf16", f"{case} layer {n} output")
+    if w.L:
+        if w.m == 0:
+            assert not s2.any()
+        else:
+            assert_scores_close(s2.cpu().numpy(), ref["scores"], f"{case} scores")
