@@ -202,21 +202,40 @@ ACACHE_DEVFN int tile_valid(const AttnParams& p, int j, int T_len) {
 
 // Read-slot entries of keys 4 lane .. 4 lane + 3 of key tile j: -1 where there is no key or
 // the slot lies outside the pool (flagged by `flagger` unless it marks a discarded key).
-template <bool kDrop>
-ACACHE_DEVFN void tile_slots(const AttnParams& p, int64_t kbase, int T_len, int n_kv, int j, int lane,
-                             bool flagger, int (&sl)[4]) {
+// In two steps: the loads (bit u of `keys` set where key u exists), and the checks.  Issued
+// apart, the loads' latency passes while the warp does other work.
+ACACHE_DEVFN uint32_t tile_slots_load(const AttnParams& p, int64_t kbase, int T_len, int n_kv, int j, int lane,
+                                      int (&raw)[4]) {
+    uint32_t keys = 0;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int tk = j * kBN + 4 * lane + u;
-        sl[u] = -1;
-        if (j < n_kv && tk < T_len) {
-            const int slot = p.read_slot[kbase + tk];
-            if (slot >= 0 && slot < p.num_slots)
-                sl[u] = slot;
-            else if (flagger && !(kDrop && slot == ACACHE_SLOT_NONE))
-                flag(p.dev_status, ACACHE_DEV_BAD_SLOT);
-        }
+        const bool key = j < n_kv && tk < T_len;
+        raw[u] = key ? __ldg(p.read_slot + kbase + tk) : -1;
+        keys |= (uint32_t)key << u;
     }
+    return keys;
+}
+template <bool kDrop>
+ACACHE_DEVFN void tile_slots_check(const AttnParams& p, bool flagger, uint32_t keys, const int (&raw)[4],
+                                   int (&sl)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int slot = raw[u];
+        sl[u] = -1;
+        if (!((keys >> u) & 1u)) continue;
+        if (slot >= 0 && slot < p.num_slots)
+            sl[u] = slot;
+        else if (flagger && !(kDrop && slot == ACACHE_SLOT_NONE))
+            flag(p.dev_status, ACACHE_DEV_BAD_SLOT);
+    }
+}
+template <bool kDrop>
+ACACHE_DEVFN void tile_slots(const AttnParams& p, int64_t kbase, int T_len, int n_kv, int j, int lane,
+                             bool flagger, int (&sl)[4]) {
+    int raw[4];
+    const uint32_t keys = tile_slots_load(p, kbase, T_len, n_kv, j, lane, raw);
+    tile_slots_check<kDrop>(p, flagger, keys, raw, sl);
 }
 
 // kDrop (read-slot keys only): a read-slot entry equal to ACACHE_SLOT_NONE marks a logical
@@ -270,14 +289,15 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     volatile int* abort_flag = &ctl.abort;
     int32_t* dev_status = p.dev_status;
     const long long budget = p.budget;
-    // The first key tile's read-slot entries are read by the producer lanes before the set-up
-    // below, which hides their latency (warp 12 flags bad slots; see the producers).  The maps
-    // are not written by a store grid this launch may overlap.
+    // The first key tile's read-slot entries are loaded by the producer lanes before the set-up
+    // below and checked only after it, so their latency passes during the set-up instead of
+    // holding every warp at its barrier (warp 10 flags bad slots).  The maps are not written
+    // by a store grid this launch may overlap.
     const bool prod_warp = warp >= kMmaWarp + 2;
     const bool flagger = warp == kProdWarp;
-    int sl0[4] = {-1, -1, -1, -1};
-    if (kMode == kSlotKeys && prod_warp)
-        tile_slots<kDrop>(p, kbase, T_len, n_kv, ks.entry_tile(0), lane, flagger, sl0);
+    int raw0[4] = {-1, -1, -1, -1};
+    uint32_t keys0 = 0;
+    if (kMode == kSlotKeys && prod_warp) keys0 = tile_slots_load(p, kbase, T_len, n_kv, ks.entry_tile(0), lane, raw0);
 
     // read-slot K/V stages: one arrival per producer warp of the ring (see the producers)
     constexpr int kFullArrivals = kMode == kSlotKeys ? kProdPerRing : 1;
@@ -384,6 +404,8 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     return finish(sl, rows, slot0);
                 };
                 int next[4], next_slot0;
+                int sl0[4];
+                tile_slots_check<kDrop>(p, flagger, keys0, raw0, sl0);
                 bool next_box = finish(sl0, next, next_slot0);
                 // store-then-attend: the pool rows this launch reads may have been written by the
                 // preceding store grid (launched ahead with programmatic stream serialisation).
