@@ -122,6 +122,7 @@ struct AttnParams {
     // preceding grids of the probe read)
     int early_wait;
     int n_rows, Hq, Hkv, T_len, L, P;
+    int g;                // Hq / Hkv
     float scale_log2;
     long long budget;     // cycles a pipeline wait may take before it gives up
 };
@@ -144,6 +145,11 @@ struct AttnCtl {
     float split_m[kBM];     //   chain B's row maximum (the exponent offset it used) and row sum
     float split_l[kBM];
 };
+
+// Stage and lap of ring entry e in a ring of n = 2 or 3 stages (divisions by constants).
+static_assert(kKStages == 3 && kVStages == 2, "ring sizes 2 and 3 (a third V stage with split keys)");
+ACACHE_DEVFN int ring_lap(int e, int n) { return n == 2 ? (e >> 1) : e / 3; }
+ACACHE_DEVFN int ring_stage(int e, int n) { return e - ring_lap(e, n) * n; }
 
 // Key-tile schedule of a CTA.  Ring entry e is the e-th K/V tile the producers load; chain t
 // reads its i-th key tile from entry entry(t, i).  Unsplit: every chain reads every key tile
@@ -251,14 +257,14 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
     auto sQ = [&](int t) { return base + kTileBytes * (uint32_t)t; };
     auto sK = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + s); };
     auto sV = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + kKStages + s); };
-    // CTA order: query block slowest, so the full 256-row blocks of every (request, head)
-    // start first and the ragged last blocks fill the final wave
-    const int n_bh = gridDim.x / ((p.n_rows + kQT * kBM - 1) / (kQT * kBM));   // B * Hq
-    const int bh = blockIdx.x % n_bh;
-    const int qb = blockIdx.x / n_bh;
-    const int h = bh % p.Hq;
-    const int b = bh / p.Hq;
-    const int hk = h / (p.Hq / p.Hkv);
+    // Grid (Hq, B, query blocks): the query block varies slowest, so the full 256-row blocks of
+    // every (request, head) start first and the ragged last blocks fill the final wave.  (The
+    // indices come straight from the grid: integer division costs a fresh CTA tens of cycles
+    // each.)
+    const int h = (int)blockIdx.x;
+    const int b = (int)blockIdx.y;
+    const int qb = (int)blockIdx.z;
+    const int hk = p.g == 1 ? h : h / p.g;
     // Ragged batches (read-slot keys): request b owns query rows [q_start[b], q_start[b+1]) and
     // read-slot entries [kv_start[b], kv_start[b+1]) of the flattened tensors; p.n_rows and
     // p.T_len are then the largest per-request counts.  A CTA without rows leaves at once.
@@ -416,7 +422,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 grid_launch_dependents();
                 int armed = -1;                           // last entry this warp arrived on
                 for (int e = 0; e < n_kv; ++e) {          // ring entries in load order
-                    const int s = e % nst;
+                    const int s = ring_stage(e, nst);
                     const int j = ks.entry_tile(e);           // the key tile entry e holds
                     const uint32_t dst_tile = is_v ? sVs(s) : sK(s);
                     int rows[4] = {next[0], next[1], next[2], next[3]};
@@ -424,7 +430,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     const bool box = next_box;
                     next_box = resolve(e + 1 < n_kv ? ks.entry_tile(e + 1) : n_kv, next, next_slot0);
                     if (e >= nst &&
-                        !__all_sync(0xffffffffu, wait_bar(&empty[s], ((e / nst) - 1) & 1, abort_flag, dev_status, budget)))
+                        !__all_sync(0xffffffffu, wait_bar(&empty[s], (ring_lap(e, nst) - 1) & 1, abort_flag, dev_status, budget)))
                         break;
                     // The ring's first warp announces the tile's bytes; a gather of another warp
                     // that completes first leaves the count transiently negative (allowed).  Read-
@@ -468,7 +474,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 if (*abort_flag && armed >= 0) {
                     bool landed = true;
                     for (int e = max(0, armed - nst + 1); e <= armed; ++e)
-                        landed = mbar_wait(&full[e % nst], (uint32_t)(e / nst) & 1u, kLandBudget) && landed;
+                        landed = mbar_wait(&full[ring_stage(e, nst)], (uint32_t)ring_lap(e, nst) & 1u, kLandBudget) && landed;
                     if (!__all_sync(0xffffffffu, landed) && lane == 0) ctl.unlanded = 1;
                 }
             }
@@ -501,7 +507,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 // PV_t(i) in two halves of the key tile: keys 0-63 (k steps 0-3) as soon as the
                 // softmax has published the first half of P, keys 64-127 once all of P is in
                 auto issue_pv_half = [&](int e, bool acc, int h) {
-                    const uint64_t dv = sdesc_sw128(sVs(e % n_vst), kRegion, 1024);
+                    const uint64_t dv = sdesc_sw128(sVs(ring_stage(e, n_vst)), kRegion, 1024);
 #pragma unroll
                     for (int k = 4 * h; k < 4 * h + 4; ++k)
                         umma_ts(d_o, d_s + k * 8, dv + (uint64_t)(k * 2048 / 16), idO, (acc || k > 0));
@@ -515,7 +521,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                 }
                 for (int i = 0; ok && i < nt; ++i) {
                     const int e = ks.entry(t, i);
-                    ok = wait_bar(&ctl.v_full[e % n_vst], (e / n_vst) & 1, abort_flag, dev_status, budget) &&
+                    ok = wait_bar(&ctl.v_full[ring_stage(e, n_vst)], ring_lap(e, n_vst) & 1, abort_flag, dev_status, budget) &&
                          wait_bar(&ctl.p_half[t], i & 1, abort_flag, dev_status, budget);
                     if (!ok) break;
                     tc_fence_after();
@@ -524,7 +530,7 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv_half(e, i > 0, 1);
-                    umma_commit(&ctl.v_empty[e % n_vst]);
+                    umma_commit(&ctl.v_empty[ring_stage(e, n_vst)]);
                     if (i + 1 < nt) {
                         const int en = ks.entry(t, i + 1);
                         ok = wait_bar(&ctl.k_full[en % kKStages], (en / kKStages) & 1, abort_flag, dev_status, budget);
@@ -1297,21 +1303,23 @@ int launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned threads, uint32_t
 // a store (store-then-attend; prm.early_wait orders the pool reads after it) or the attention
 // of another layer (chained layers; prm.early_wait = 0).
 template <int kMode, bool kDrop = false>
-int launch_attn(const AttnParams& prm, int B, cudaStream_t stream, bool pdl = false) {
-    const int64_t ctas = (int64_t)B * prm.Hq * ((prm.n_rows + kQT * kBM - 1) / (kQT * kBM));
-    if (ctas == 0) return ACACHE_OK;
-    if (ctas > 0x7fffffff) return ACACHE_ERR_INVALID_ARG;
+int launch_attn(AttnParams prm, int B, cudaStream_t stream, bool pdl = false) {
+    const int64_t n_qb = (prm.n_rows + kQT * kBM - 1) / (kQT * kBM);
+    if ((int64_t)B * prm.Hq * n_qb == 0) return ACACHE_OK;
+    if (B > 65535 || n_qb > 65535) return ACACHE_ERR_INVALID_ARG;
+    const dim3 grid((unsigned)prm.Hq, (unsigned)B, (unsigned)n_qb);
+    prm.g = prm.Hq / prm.Hkv;
     auto kern = tc_attn_kernel<kMode, kDrop>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return ACACHE_ERR_CUDA;
     }
     if (!pdl) {
-        kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(prm);
+        kern<<<grid, kThreads, kSmemBytes, stream>>>(prm);
         return launch_status();
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
