@@ -319,6 +319,38 @@ def test_slot_attention_parity(dtype, d, heads, n_q, T):
     assert_out_close(out.float().cpu().numpy(), ref, dtype, "slot attention")
 
 
+# More CTAs (256-row query blocks of a request and head) than SMs, so the grid runs in several
+# waves, with GQA and MHA heads.  (B, n_q, Hq, Hkv, T): two-tile blocks followed by one-tile
+# blocks whose keys the two chains split; one key tile only (the one-tile blocks then have a
+# single chain); the fewest key tiles a split takes (2, 3); four to five waves; one-tile blocks
+# only.
+WAVE_CASES = [
+    (4, 600, 32, 8, 700),
+    (4, 300, 32, 32, 100),
+    (4, 300, 32, 4, 200),
+    (2, 1100, 64, 8, 300),
+    (8, 100, 32, 8, 500),
+]
+
+
+@pytest.mark.parametrize("B,n_q,hq,hkv,T", WAVE_CASES)
+def test_slot_attention_more_blocks_than_sms(B, n_q, hq, hkv, T):
+    d, num_slots = 128, 3000
+    g = torch.Generator().manual_seed(B * 100 + n_q + hq + T)
+    kc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
+    q = (torch.randn((B, n_q, hq, d), generator=g) * 2).to(torch.bfloat16)
+    rs = torch.randint(0, num_slots, (B, T), generator=g, dtype=torch.int32)
+    ref = oracle.slot_attention(q, rs, kc, vc, scale=d ** -0.5)
+    out = torch.full((B, n_q, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = status_tensor()
+    ac.acache_slot_attention(ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16"), B, n_q, dev(q), T, dev(rs),
+                             dev(kc), dev(vc), num_slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(out.float().cpu().numpy(), ref, "bf16", "slot attention, several waves")
+
+
 # Few query rows per KV head (the block-decode step): (B, n_q, Hq, Hkv, T).  The cases span
 # 4 / 2 / 1 replicas of the packed rows, key ranges split over clusters of 1, 2 and 4 CTAs,
 # GQA groups packed into one or two row blocks, and ragged last key tiles.

@@ -18,9 +18,9 @@ from gpu_helpers import assert_out_close, dev, status_tensor
 pytestmark = pytest.mark.gpu
 
 
-def _case():
+def _case(B=2, n_q=300, T=700, hq=4, hkv=2):
     g = torch.Generator().manual_seed(77)
-    B, n_q, T, hq, hkv, d, num_slots = 2, 300, 700, 4, 2, 128, 1500
+    d, num_slots = 128, 1500
     kc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
     vc = torch.randn((num_slots, hkv, d), generator=g).to(torch.bfloat16)
     q = torch.randn((B, n_q, hq, d), generator=g).to(torch.bfloat16)
@@ -28,8 +28,10 @@ def _case():
     return B, n_q, T, hq, hkv, d, num_slots, kc, vc, q, rs
 
 
-def test_wait_that_runs_out_flags_timeout_and_leaves_the_context_usable():
-    B, n_q, T, hq, hkv, d, num_slots, kc, vc, q, rs = _case()
+# (B, n_q, T, Hq, Hkv): one wave of CTAs; several waves (384 CTAs)
+@pytest.mark.parametrize("shape", [(2, 300, 700, 4, 2), (4, 600, 700, 32, 8)])
+def test_wait_that_runs_out_flags_timeout_and_leaves_the_context_usable(shape):
+    B, n_q, T, hq, hkv, d, num_slots, kc, vc, q, rs = _case(*shape)
     desc = ac.attn_desc(hq, hkv, d, d ** -0.5, "bf16")
     args = (desc, B, n_q, dev(q), T, dev(rs), dev(kc), dev(vc), num_slots)
     out = torch.zeros((B, n_q, hq, d), dtype=torch.bfloat16, device="cuda")
