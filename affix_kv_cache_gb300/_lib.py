@@ -27,6 +27,7 @@ ACACHE_BF16 = 1
 ACACHE_PATH_RECOMPUTE = 0
 ACACHE_PATH_BLOCK_DECODE = 1
 ACACHE_PATH_CUDA_CORES = 2
+ACACHE_PATH_RECOMPUTE_PERSISTENT = 3
 SLOT_NONE = -1
 DEV_BAD_SLOT, DEV_SHARED_WRITE, DEV_BAD_ROW, DEV_BAD_ANCHOR, DEV_NAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
 DEV_BAD_LENGTH = 64
@@ -255,7 +256,8 @@ def acache_slot_attention_dropna(desc, batch, n_q, q, seq_len, read_slot, k_cach
 
 def acache_slot_attention_path(desc, batch, n_q, seq_len) -> int:
     """The kernel acache_slot_attention runs for this geometry: ACACHE_PATH_RECOMPUTE,
-    ACACHE_PATH_BLOCK_DECODE or ACACHE_PATH_CUDA_CORES (see include/acache.h)."""
+    ACACHE_PATH_RECOMPUTE_PERSISTENT, ACACHE_PATH_BLOCK_DECODE or ACACHE_PATH_CUDA_CORES (see
+    include/acache.h)."""
     st = int(lib().acache_slot_attention_path(ctypes.byref(desc), batch, n_q, seq_len))
     return _check("acache_slot_attention_path", st) if st < 0 else st
 

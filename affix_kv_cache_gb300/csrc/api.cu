@@ -305,7 +305,8 @@ int acache_slot_attention_path(const acache_attn_desc* desc, int batch, int n_q,
     if (int rc = check_desc(desc, &a)) return rc;
     if (batch < 0 || n_q < 0 || seq_len < 0) return ACACHE_ERR_INVALID_ARG;
     if (!tc_supported(a)) return ACACHE_PATH_CUDA_CORES;
-    return tc_decode_preferred(a, batch, n_q, seq_len) ? ACACHE_PATH_BLOCK_DECODE : ACACHE_PATH_RECOMPUTE;
+    if (tc_decode_preferred(a, batch, n_q, seq_len)) return ACACHE_PATH_BLOCK_DECODE;
+    return tc_slot_persistent(a, batch, n_q, seq_len) ? ACACHE_PATH_RECOMPUTE_PERSISTENT : ACACHE_PATH_RECOMPUTE;
 }
 
 int acache_topk_anchors(const float* scores, int batch, int affix_len, int k, int32_t* anchors,

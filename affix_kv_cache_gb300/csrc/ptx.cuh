@@ -136,6 +136,13 @@ ACACHE_DEVFN void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1, i
 ACACHE_DEVFN void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has read its shared-memory source.
 ACACHE_DEVFN void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Brings the box at these coordinates of a 4-D tensor map into L2 (no shared memory, no
+// completion to wait for).
+ACACHE_DEVFN void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
 ACACHE_DEVFN void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

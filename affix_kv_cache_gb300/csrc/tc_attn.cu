@@ -59,6 +59,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "tc_attn.cuh"
 #include "ptx.cuh"
@@ -123,6 +124,8 @@ struct AttnParams {
     int early_wait;
     int n_rows, Hq, Hkv, T_len, L, P;
     int g;                // Hq / Hkv
+    int B;                // requests (persistent launch)
+    int n_kv, n_units;    // persistent launch: key tiles (<= 16), units (< 2^22)
     float scale_log2;
     long long budget;     // cycles a pipeline wait may take before it gives up
 };
@@ -804,6 +807,575 @@ tc_attn_kernel(const __grid_constant__ AttnParams p) {
 }
 
 // ------------------------------------------------------------------------------------------
+// Persistent read-slot attention (the slot_attn step of the ACache page: every logical position
+// reads its K/V through the request's read-slot map), for a batch of equal-length requests with
+// no discarded keys, when there are more units than SMs.  tc_attn_kernel starts one CTA per
+// 256-row query block of a (request, head), and each pays for starting a fresh CTA, filling its
+// rings and draining its last tiles.  Here one CTA per SM works through units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  A unit is the work of one tc_attn_kernel CTA, taken in that
+// kernel's grid order.  Every ring and barrier carries on from one unit into the next:
+//   - the producers load the next unit's first K/V tiles while the current unit finishes;
+//   - each chain's next Q tile is prefetched into L2 while the unit runs, and loaded once the
+//     epilogue's store has read the rows staged in its buffer;
+//   - chain A starts its next unit while chain B, a turn behind, finishes the current one.
+//
+// Ring accounting is uniform: both chains release every K and V entry.  A chain that does not
+// read an entry releases it as soon as it has landed.  Such entries are the other chain's half
+// of split keys, and every entry of the idle chain in a unit with one Q tile and one key tile.
+// So each chain waits for every entry in ring order, and no barrier phase goes by unseen.
+//
+// With split keys both Q buffers hold the unit's tile, one per chain, so each buffer is loaded
+// and read by one chain only.  Every barrier gets one phase per unit (drain, Q), per tile (S,
+// P, turn) or per split unit (the hand-off), and each is waited in order.
+struct PersistCtl {
+    uint64_t q_full[kQT];         // Q buffer t holds the unit's tile (a bare phase when it has none)
+    uint64_t k_full[kKStages];
+    uint64_t k_empty[kKStages];
+    uint64_t v_full[kVStages];
+    uint64_t v_empty[kVStages];
+    uint64_t s_full[kQT];
+    uint64_t p_half[kQT];
+    uint64_t p_full[kQT];
+    uint64_t turn[kQT];
+    uint64_t drain[kQT];          // chain t's MMAs of the unit are complete
+    uint64_t split_ready;         // split keys: chain B's row statistics are written,
+    uint64_t split_done;          //   and chain A has read them and O_B
+    uint64_t fin[kQT];            // end of the kernel: chain t's MMAs are complete
+    uint32_t tmem_base;
+    int abort;
+    int unlanded;
+    uint32_t q_last[kQT];         // parity of the last phase issued on q_full[t] (abort path: it may be in flight)
+    float split_m[kBM];
+    float split_l[kBM];
+};
+
+// Unit u of a persistent launch: query block (slowest), request, query head.
+struct PUnit {
+    int h, b, hk, q0, n_qt;
+    KeySchedule ks;
+    ACACHE_DEVFN int n_ch() const { return ks.split ? 2 : n_qt; }
+    ACACHE_DEVFN int nt(int t) const { return t < n_ch() ? ks.n_tiles(t) : 0; }
+};
+ACACHE_DEVFN PUnit punit(const AttnParams& p, int u, int n_kv) {
+    PUnit w;
+    const int bhq = p.B * p.Hq;
+    const int qb = u / bhq, bh = u - qb * bhq;
+    w.b = bh / p.Hq;
+    w.h = bh - w.b * p.Hq;
+    w.hk = p.g == 1 ? w.h : w.h / p.g;
+    w.q0 = qb * kQT * kBM;
+    w.n_qt = min(kQT, (p.n_rows - w.q0 + kBM - 1) / kBM);
+    const bool split = w.n_qt == 1 && n_kv >= 2;
+    w.ks = KeySchedule{split, n_kv, split ? (n_kv + 1) / 2 : n_kv};
+    return w;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_slot_persist_kernel(const __grid_constant__ AttnParams p) {
+    extern __shared__ uint8_t dsm[];
+    __shared__ PersistCtl ctl;
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    // shared memory: Q_A, Q_B, the K ring, the V ring (32 KB tiles, 1024-byte aligned)
+    auto sQ = [&](int t) { return base + kTileBytes * (uint32_t)t; };
+    auto sK = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + s); };
+    auto sV = [&](int s) { return base + kTileBytes * (uint32_t)(kQT + kKStages + s); };
+    const int n_kv = p.n_kv;
+    const int n_units = p.n_units;
+    const int u_first = (int)blockIdx.x, u_step = (int)gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
+    // (the pipeline waits take their abort flag, status word and budget straight from shared and
+    // parameter memory: held in registers they would crowd the 48-register roles)
+    volatile int* abort_flag = &ctl.abort;
+    // Q buffer t of unit w: its tile t, with split keys a copy of its one tile, else a bare phase
+    auto load_q = [&](const PUnit& w, int t) {
+        if (t < w.n_qt || w.ks.split) {
+            const int row = w.q0 + (w.ks.split ? 0 : t) * kBM;
+            mbar_arrive_expect_tx(&ctl.q_full[t], kTileBytes);
+            tma_load_4d(sQ(t), &p.tm_q, 0, w.h, row, w.b, &ctl.q_full[t]);
+            tma_load_4d(sQ(t) + kRegion, &p.tm_q, 64, w.h, row, w.b, &ctl.q_full[t]);
+        } else {
+            mbar_arrive(&ctl.q_full[t]);
+        }
+    };
+    // The producers load the read-slot entries of the first unit's first key tile before the set-
+    // up and check them after it (as tc_attn_kernel does): their latency passes meanwhile.
+    int raw0[4] = {-1, -1, -1, -1};
+    uint32_t keys0 = 0;
+    if (warp >= kMmaWarp + 2) {
+        const int b0 = (u_first % (p.B * p.Hq)) / p.Hq;
+        keys0 = tile_slots_load(p, (int64_t)b0 * p.T_len, p.T_len, n_kv, 0, lane, raw0);
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&ctl.k_full[s], kProdPerRing);
+            mbar_init(&ctl.k_empty[s], kQT);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&ctl.v_full[s], kProdPerRing);
+            mbar_init(&ctl.v_empty[s], kQT);
+        }
+        for (int t = 0; t < kQT; ++t) {
+            mbar_init(&ctl.q_full[t], 1);
+            mbar_init(&ctl.s_full[t], 1);
+            mbar_init(&ctl.p_half[t], 128);
+            mbar_init(&ctl.p_full[t], 128);
+            mbar_init(&ctl.turn[t], 128);
+            mbar_init(&ctl.drain[t], 1);
+            mbar_init(&ctl.fin[t], 1);
+            ctl.q_last[t] = 0;
+        }
+        mbar_init(&ctl.split_ready, 128);
+        mbar_init(&ctl.split_done, 128);
+        ctl.abort = 0;
+        ctl.unlanded = 0;
+        fence_mbar_init();
+        const PUnit w0 = punit(p, u_first, n_kv);     // gridDim.x <= the number of units
+        load_q(w0, 0);
+        load_q(w0, 1);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ctl.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    if (wg >= 2) {
+        setmaxnreg_dec<kRegOther>();
+        if (warp >= kMmaWarp + 2) {
+            // -------------------------------------------------------------- TMA producers
+            // (as in tc_attn_kernel: kProdPerRing warps per ring, one arrival per warp and entry,
+            // read-slot tiles resolved one entry ahead -- here across unit boundaries too)
+            if (warp == kProdWarp && lane == 0) {
+                tma_prefetch_desc(&p.tm_o);
+                tma_prefetch_desc(&p.tm_k0);
+                tma_prefetch_desc(&p.tm_v0);
+                tma_prefetch_desc(&p.tm_k1);
+                tma_prefetch_desc(&p.tm_v1);
+            }
+            const bool is_v = warp >= kProdWarp + kProdPerRing;
+            const int pi = warp - kProdWarp - (is_v ? kProdPerRing : 0);
+            const int nst = is_v ? kVStages : kKStages;
+            uint64_t* full = is_v ? ctl.v_full : ctl.k_full;
+            uint64_t* empty = is_v ? ctl.v_empty : ctl.k_empty;
+            const CUtensorMap* tm_rows = is_v ? &p.tm_v0 : &p.tm_k0;   // pool rows (gather4)
+            const CUtensorMap* tm_box = is_v ? &p.tm_v1 : &p.tm_k1;    // pool [slot][Hkv][d] (boxes)
+            const bool leader = pi == 0 && lane == 0;
+            const bool flagger = warp == kProdWarp;
+            const int oob_row = (int)(p.num_slots * p.Hkv);
+            const int x = kProdPerRing * lane + pi;
+            const bool gathers = x < 64;
+            const int g = x >> 1, half = x & 1;
+            auto finish = [&](const int (&sl)[4], int hk, int (&rows)[4], int& slot0) -> bool {
+                bool run = sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 && sl[3] == sl[0] + 3;
+                const int after = __shfl_down_sync(0xffffffffu, sl[0], 1);
+                if (lane < 31) run = run && after == sl[0] + 4;
+                slot0 = __shfl_sync(0xffffffffu, sl[0], 0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int sv = __shfl_sync(0xffffffffu, sl[q], g & 31);
+                    rows[q] = (gathers && sv >= 0) ? sv * p.Hkv + hk : oob_row;
+                }
+                return __all_sync(0xffffffffu, run);
+            };
+            auto resolve = [&](const PUnit& w, int j, int (&rows)[4], int& slot0) -> bool {
+                int sl[4];
+                tile_slots<false>(p, (int64_t)w.b * p.T_len, p.T_len, n_kv, j, lane, flagger, sl);
+                return finish(sl, w.hk, rows, slot0);
+            };
+            int u = u_first, e = 0;
+            PUnit w = punit(p, u, n_kv);
+            int next[4], next_slot0;
+            int sl0[4];
+            tile_slots_check<false>(p, flagger, keys0, raw0, sl0);
+            bool next_box = finish(sl0, w.hk, next, next_slot0);
+            // store-then-attend: the pool may have been written by the preceding grid
+            if (p.early_wait == 1) grid_dependency_wait();
+            grid_launch_dependents();
+            int armed = -1;                                   // last entry this warp arrived on
+            for (int eg = 0; u < n_units; ++eg) {             // ring entries in load order
+                const int s = ring_stage(eg, nst);
+                const uint32_t dst = is_v ? sV(s) : sK(s);
+                const int rows[4] = {next[0], next[1], next[2], next[3]};
+                const int slot0 = next_slot0, hk = w.hk;
+                const bool box = next_box;
+                if (++e == n_kv) {
+                    e = 0;
+                    u += u_step;
+                    if (u < n_units) w = punit(p, u, n_kv);
+                }
+                if (u < n_units) next_box = resolve(w, w.ks.entry_tile(e), next, next_slot0);
+                if (eg >= nst &&
+                    !__all_sync(0xffffffffu, wait_bar(&empty[s], (ring_lap(eg, nst) - 1) & 1, &ctl.abort, p.dev_status, p.budget)))
+                    break;
+                if (leader) mbar_arrive_expect_tx(&full[s], kTileBytes);
+                else if (lane == 0) mbar_arrive(&full[s]);
+                armed = eg;
+                __syncwarp();
+                if (box) {
+                    if (leader) {
+                        tma_load_3d(dst, tm_box, 0, hk, slot0, &full[s]);
+                        tma_load_3d(dst + kRegion, tm_box, 64, hk, slot0, &full[s]);
+                    }
+                } else if (gathers) {
+                    tma_gather4(dst + (uint32_t)half * kRegion + (uint32_t)g * 512u, tm_rows, half * 64, rows[0],
+                                rows[1], rows[2], rows[3], &full[s]);
+                }
+            }
+            // abort: the loads this warp issued land before the CTA exits (see tc_attn_kernel)
+            if (*abort_flag && armed >= 0) {
+                bool landed = true;
+                for (int a = max(0, armed - nst + 1); a <= armed; ++a)
+                    landed = mbar_wait(&full[ring_stage(a, nst)], (uint32_t)ring_lap(a, nst) & 1u, kLandBudget) && landed;
+                if (!__all_sync(0xffffffffu, landed) && lane == 0) ctl.unlanded = 1;
+            }
+        } else {
+            // ------------------------------------------------------------------ MMA issuers
+            // (as in tc_attn_kernel; chain t reads Q buffer t in every unit).  Compiled once per
+            // chain, so the chain's barriers, buffers and TMEM columns are constants.
+            auto mma_role = [&](auto chain) {
+                constexpr int t = decltype(chain)::value;
+                const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+                const uint32_t idO = idesc_bf16(kBM, kD, false, true);
+                const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
+                const uint64_t dq = sdesc_sw128(sQ(t), 16, 1024);
+                auto issue_s = [&](int eg) {
+                    const uint64_t dk = sdesc_sw128(sK(ring_stage(eg, kKStages)), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint64_t ko = ((uint64_t)(kk >> 2) * kRegion + (uint64_t)(kk & 3) * 32u) >> 4;
+                        umma_ss(d_s, dq + ko, dk + ko, idS, kk > 0);
+                    }
+                    umma_commit(&ctl.s_full[t]);
+                    umma_commit(&ctl.k_empty[ring_stage(eg, kKStages)]);
+                };
+                auto issue_pv_half = [&](int eg, bool acc, int hh) {
+                    const uint64_t dv = sdesc_sw128(sV(eg & 1), kRegion, 1024);
+#pragma unroll
+                    for (int kk = 4 * hh; kk < 4 * hh + 4; ++kk)
+                        umma_ts(d_o, d_s + kk * 8, dv + (uint64_t)(kk * 2048 / 16), idO, (acc || kk > 0));
+                };
+                // parity bit 0 counts this chain's tiles (P), bit 1 the units (Q); E the ring
+                // entries of the units before
+                uint32_t ph = 0;
+                int E = 0;
+                for (int u = u_first; u < n_units; u += u_step) {
+                    int nt, n0;
+                    bool split;
+                    {
+                        const PUnit w = punit(p, u, n_kv);
+                        nt = w.nt(t);
+                        n0 = w.ks.n0;
+                        split = w.ks.split;
+                    }
+                    // Entries this chain does not read are released once landed.  Unsplit units:
+                    // both chains read every entry (the idle chain of a one-tile unit, which then
+                    // has one key tile, reads none).  Split keys (KeySchedule): the entries alternate
+                    // chain A, chain B, chain A's extra tile (odd n_kv) last, so the entry before
+                    // each of this chain's own is the other chain's -- released (K before the S, V
+                    // before the PV) -- and so is the last entry if this chain does not own it.
+                    const int n1 = n_kv - n0;
+                    auto entry = [&](int i) { return split ? (i < n1 ? 2 * i + t : n1 + i) : i; };
+                    auto rel_k = [&](int eg) -> bool {
+                        if (!wait_bar(&ctl.k_full[ring_stage(eg, kKStages)], ring_lap(eg, kKStages) & 1, &ctl.abort,
+                                      p.dev_status, p.budget))
+                            return false;
+                        mbar_arrive(&ctl.k_empty[ring_stage(eg, kKStages)]);
+                        return true;
+                    };
+                    auto rel_v = [&](int eg) -> bool {
+                        if (!wait_bar(&ctl.v_full[eg & 1], (eg >> 1) & 1, &ctl.abort, p.dev_status, p.budget))
+                            return false;
+                        mbar_arrive(&ctl.v_empty[eg & 1]);
+                        return true;
+                    };
+                    bool ok = wait_bar(&ctl.q_full[t], (ph >> 1) & 1u, &ctl.abort, p.dev_status, p.budget);
+                    if (ok && nt > 0) {
+                        const int e0 = entry(0);
+                        ok = (!split || e0 == 0 || rel_k(E + e0 - 1)) &&
+                             wait_bar(&ctl.k_full[ring_stage(E + e0, kKStages)], ring_lap(E + e0, kKStages) & 1,
+                                      &ctl.abort, p.dev_status, p.budget);
+                        if (ok) {
+                            tc_fence_after();
+                            issue_s(E + e0);
+                        }
+                        for (int i = 0; ok && i < nt; ++i) {
+                            const int e = entry(i), eg = E + e;
+                            const uint32_t pp = (ph ^ (uint32_t)i) & 1u;
+                            ok = (!split || e == 0 || rel_v(eg - 1)) &&
+                                 wait_bar(&ctl.v_full[eg & 1], (eg >> 1) & 1, &ctl.abort, p.dev_status, p.budget) &&
+                                 wait_bar(&ctl.p_half[t], pp, &ctl.abort, p.dev_status, p.budget);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv_half(eg, i > 0, 0);
+                            ok = wait_bar(&ctl.p_full[t], pp, &ctl.abort, p.dev_status, p.budget);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv_half(eg, i > 0, 1);
+                            umma_commit(&ctl.v_empty[eg & 1]);
+                            if (i + 1 < nt) {
+                                const int egn = E + entry(i + 1);
+                                ok = (!split || rel_k(egn - 1)) &&
+                                     wait_bar(&ctl.k_full[ring_stage(egn, kKStages)], ring_lap(egn, kKStages) & 1,
+                                              &ctl.abort, p.dev_status, p.budget);
+                                if (!ok) break;
+                                tc_fence_after();
+                                issue_s(egn);
+                            }
+                        }
+                        // split keys: the last entry, if the other chain's
+                        if (ok && split && ((n_kv & 1) == t)) ok = rel_k(E + n_kv - 1) && rel_v(E + n_kv - 1);
+                    } else if (ok) {
+                        // idle chain: every entry (one key tile)
+                        for (int e = 0; ok && e < n_kv; ++e) ok = rel_k(E + e) && rel_v(E + e);
+                    }
+                    if (!ok) break;
+                    umma_commit(&ctl.drain[t]);
+                    E += n_kv;
+                    ph ^= (uint32_t)(nt & 1) | 2u;
+                }
+                // no MMA may still run when TMEM is released
+                umma_commit(&ctl.fin[t]);
+                mbar_wait(&ctl.fin[t], 0, kDrainBudget);
+            };
+            if (lane == 0) {
+                if (warp == kMmaWarp) mma_role(std::integral_constant<int, 0>{});
+                else mma_role(std::integral_constant<int, 1>{});
+            }
+            __syncwarp();
+        }
+    } else {
+        setmaxnreg_inc<kRegSoftmax>();
+        // ------------------------------------------------------------------ softmax + epilogue
+        // (the tile loop is tc_attn_kernel's; phases count on across units)
+        const int t = wg;
+        const int r = threadIdx.x - t * 128;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float c = p.scale_log2;
+        const uint32_t stage = sQ(t);
+        // Barrier phases are used by parity only: bit 0 counts this chain's tiles (S, P), bits 1
+        // and 2 chain A's and chain B's tiles of ping-pong units (turns), bit 3 the units (drain),
+        // bit 4 the split units (hand-off).
+        // (the unit and the parity bits share one register, u << 5 | bits, and the unit's tile
+        // count, first key tile and ping-pong flag another: few values stay live through the
+        // tile loop, whose S tile fills most of the softmax warps' registers)
+        for (uint32_t su = (uint32_t)u_first << 5; (int)(su >> 5) < n_units; su += (uint32_t)u_step << 5) {
+            const int u = (int)(su >> 5);
+            uint32_t cfg;      // bits 0-15 tiles of this chain, 16-30 its first key tile, 31 ping-pong
+            {
+                const PUnit w = punit(p, u, n_kv);
+                cfg = (uint32_t)w.nt(t) | (uint32_t)((w.ks.split && t == 1) ? w.ks.n0 : 0) << 16 |
+                      (w.n_ch() > 1 ? 0x80000000u : 0u);
+            }
+            const int un = u + u_step;
+            // the next unit's Q tile of this buffer into L2 while this unit runs
+            if (r == 0 && un < n_units) {
+                const PUnit wn = punit(p, un, n_kv);
+                if (t < wn.n_qt || wn.ks.split) {
+                    const int row = wn.q0 + (wn.ks.split ? 0 : t) * kBM;
+                    tma_prefetch_l2_4d(&p.tm_q, 0, wn.h, row, wn.b);
+                    tma_prefetch_l2_4d(&p.tm_q, 64, wn.h, row, wn.b);
+                }
+            }
+            float m_used = -INFINITY, l_sum = 0.f;
+            bool ok = true;
+            const int nt = (int)(cfg & 0xffffu);
+            for (int i = 0; i < nt; ++i) {
+                const int j = (int)((cfg >> 16) & 0x7fffu) + i;
+                ok = __all_sync(0xffffffffu, wait_bar(&ctl.s_full[t], (su ^ (uint32_t)i) & 1u, &ctl.abort, p.dev_status, p.budget));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t v[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_base + col_s(t) + cc * 32, v[cc]);
+                tmem_ld_wait();
+                if ((cfg >> 31) && (t == 1 || i > 0))
+                    ok = __all_sync(0xffffffffu, wait_bar(&ctl.turn[t], ((t == 0 ? (su >> 2) ^ 1u : su >> 1) ^ (uint32_t)i) & 1u,
+                                                          &ctl.abort, p.dev_status, p.budget));
+                if (!ok) break;
+                const int valid = min(kBN, p.T_len - j * kBN);
+                if (valid < kBN) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            if (cc * 32 + q >= valid) v[cc][q] = __float_as_uint(-INFINITY);
+                }
+                float mx[4];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    mx[cc] = max3f(__uint_as_float(v[cc][0]), __uint_as_float(v[cc][1]), __uint_as_float(v[cc][2]));
+#pragma unroll
+                    for (int q = 3; q < 31; q += 2)
+                        mx[cc] = max3f(mx[cc], __uint_as_float(v[cc][q]), __uint_as_float(v[cc][q + 1]));
+                    mx[cc] = fmaxf(mx[cc], __uint_as_float(v[cc][31]));
+                }
+                const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
+                float alpha = 1.f;
+                bool resc = false;
+                if (i == 0) {
+                    m_used = mt;
+                } else if (mt > m_used + kRescaleThreshold) {
+                    alpha = fast_exp2(m_used - mt);
+                    m_used = mt;
+                    resc = true;
+                }
+                if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int q = 0; q < kD / 8; ++q) {
+                        uint32_t o[8];
+                        tmem_ld8(lane_base + col_o(t) + q * 8, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int xx = 0; xx < 8; ++xx) o[xx] = __float_as_uint(__uint_as_float(o[xx]) * alpha);
+                        tmem_st8(lane_base + col_o(t) + q * 8, o);
+                    }
+                    tmem_st_wait();
+                }
+                const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_used, -m_used);
+                uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int q = 0; q < 32; q += 2) {
+                        float x0, x1;
+                        f2unpack(f2fma(f2pack(__uint_as_float(v[cc][q]), __uint_as_float(v[cc][q + 1])), c2, nm2),
+                                 x0, x1);
+                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                        ls2[(q >> 1) & 1] = f2add(ls2[(q >> 1) & 1], f2pack(p0, p1));
+                        __nv_bfloat162 two = __floats2bfloat162_rn(p0, p1);
+                        pk[q >> 1] = *reinterpret_cast<uint32_t*>(&two);
+                    }
+                    tmem_st16(lane_base + col_s(t) + cc * 16, pk);
+                    if (cc == 1) {
+                        tmem_st_wait();
+                        tc_fence_before();
+                        mbar_arrive(&ctl.p_half[t]);
+                    }
+                }
+                float l0, l1, l2, l3;
+                f2unpack(ls2[0], l0, l1);
+                f2unpack(ls2[1], l2, l3);
+                l_sum = l_sum * alpha + ((l0 + l1) + (l2 + l3));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&ctl.p_full[t]);
+                if (cfg >> 31) mbar_arrive(&ctl.turn[t ^ 1]);
+            }
+            // drain[t] is committed after the chain's last MMA of the unit (once per unit, also
+            // when the chain has no tile); then Q buffer t is free
+            if (ok) ok = __all_sync(0xffffffffu, wait_bar(&ctl.drain[t], (su >> 3) & 1u, &ctl.abort, p.dev_status, p.budget));
+            // the unit's indices again (recomputed rather than held through the tile loop)
+            int u2 = (int)(su >> 5);
+            asm volatile("" : "+r"(u2));
+            const PUnit w = punit(p, u2, n_kv);
+            // Split keys: chain B hands its row statistics to chain A (split_ready) and waits
+            // until A has read them and O_B (split_done) before its next tile may overwrite O_B.
+            float w_a = 1.f, w_b = 0.f;
+            if (w.ks.split) {
+                if (t == 1) {
+                    ctl.split_m[r] = m_used;
+                    ctl.split_l[r] = l_sum;
+                    mbar_arrive(&ctl.split_ready);
+                } else if (ok) {
+                    ok = __all_sync(0xffffffffu, wait_bar(&ctl.split_ready, (su >> 4) & 1u, &ctl.abort, p.dev_status, p.budget)) &&
+                         !*abort_flag &&
+                         __all_sync(0xffffffffu, wait_bar(&ctl.drain[1], (su >> 3) & 1u, &ctl.abort, p.dev_status, p.budget));
+                    if (ok) {
+                        const float mb = ctl.split_m[r], lb = ctl.split_l[r];
+                        const float m = fmaxf(m_used, mb);
+                        w_a = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m);
+                        w_b = mb == -INFINITY ? 0.f : fast_exp2(mb - m);
+                        l_sum = l_sum * w_a + lb * w_b;
+                    }
+                }
+            }
+            // The rows, normalised, leave through this chain's Q buffer and two tensor-map stores
+            // (as in tc_attn_kernel); the buffer then takes the next unit's Q tile.
+            const bool writer = nt > 0 && (!w.ks.split || t == 0);
+            if (writer && ok) {
+                tc_fence_after();
+                const float inv_l = 1.f / l_sum;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + col_o(t) + cc * 32, o);
+                    tmem_ld_wait();
+                    if (w.ks.split) {
+                        uint32_t ob[32];
+                        tmem_ld32(lane_base + col_o(1) + cc * 32, ob);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int xx = 0; xx < 32; ++xx)
+                            o[xx] = __float_as_uint(fmaf(__uint_as_float(o[xx]), w_a, __uint_as_float(ob[xx]) * w_b));
+                    }
+                    uint32_t pkd[16];
+#pragma unroll
+                    for (int xx = 0; xx < 16; ++xx) {
+                        __nv_bfloat162 two = __floats2bfloat162_rn(__uint_as_float(o[2 * xx]) * inv_l,
+                                                                   __uint_as_float(o[2 * xx + 1]) * inv_l);
+                        pkd[xx] = *reinterpret_cast<uint32_t*>(&two);
+                    }
+#pragma unroll
+                    for (int xx = 0; xx < 4; ++xx) {
+                        const int kc = 4 * cc + xx;
+                        st_shared_v4(stage + (uint32_t)(kc >> 3) * kRegion + (uint32_t)r * 128u +
+                                         ((uint32_t)((kc & 7) ^ (r & 7)) << 4),
+                                     pkd[4 * xx], pkd[4 * xx + 1], pkd[4 * xx + 2], pkd[4 * xx + 3]);
+                    }
+                }
+            }
+            if (w.ks.split) {
+                if (t == 0) {
+                    tc_fence_before();
+                    mbar_arrive(&ctl.split_done);
+                } else if (ok) {
+                    ok = __all_sync(0xffffffffu, wait_bar(&ctl.split_done, (su >> 4) & 1u, &ctl.abort, p.dev_status, p.budget));
+                }
+            }
+            if (writer) fence_proxy_async_smem();
+            // every thread of the warpgroup takes part in every unit's vote, so its four warps
+            // leave the loop together
+            const bool all_ok = t == 0 ? named_barrier_and<2>(kBM, ok) : named_barrier_and<3>(kBM, ok);
+            if (r == 0 && all_ok) {
+                if (writer) {
+                    const int row = w.q0 + (w.ks.split ? 0 : t) * kBM;
+                    tma_store_4d(&p.tm_o, stage, 0, w.h, row, w.b);
+                    tma_store_4d(&p.tm_o, stage + kRegion, 64, w.h, row, w.b);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
+                if (un < n_units) {
+                    load_q(punit(p, un, n_kv), t);
+                    ctl.q_last[t] = ((su >> 3) & 1u) ^ 1u;
+                }
+            }
+            if (!all_ok) break;
+            su ^= (uint32_t)(w.nt(t) & 1) | 8u | (w.ks.split ? 16u : 0u);
+            if (w.n_ch() > 1) su ^= (uint32_t)((w.nt(0) & 1) << 1 | (w.nt(1) & 1) << 2);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (*abort_flag) {
+        // the last Q load issued on each buffer lands before the CTA exits (an earlier one was
+        // waited for before the next was issued)
+        if (threadIdx.x == 0)
+            for (int t = 0; t < kQT; ++t)
+                if (!mbar_wait(&ctl.q_full[t], ctl.q_last[t], kLandBudget)) ctl.unlanded = 1;
+        __syncthreads();
+        settle_after_abort(ctl.unlanded != 0);
+    }
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+    // a chained layer waits for the grid before it before its CTAs exit (see tc_attn_kernel)
+    if (p.early_wait != 1 && threadIdx.x == 0) grid_dependency_wait();
+}
+
+// ------------------------------------------------------------------------------------------
 // Second probe pass.
 constexpr int kCsStages = 2;
 constexpr int kCsMmaWarp = 4;
@@ -1335,9 +1907,41 @@ int launch_attn(AttnParams prm, int B, cudaStream_t stream, bool pdl = false) {
     return launch_status();
 }
 
+// The persistent kernel: one CTA per SM.
+int launch_attn_persist(AttnParams prm, int B, cudaStream_t stream, bool pdl) {
+    const int64_t n_units = (int64_t)B * prm.Hq * ((prm.n_rows + kQT * kBM - 1) / (kQT * kBM));
+    prm.g = prm.Hq / prm.Hkv;
+    prm.B = B;
+    prm.n_kv = (prm.T_len + kBN - 1) / kBN;
+    prm.n_units = (int)n_units;
+    const unsigned grid = (unsigned)std::min<int64_t>(n_units, sm_count());
+    if (cudaFuncSetAttribute(tc_slot_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return ACACHE_ERR_CUDA;
+    }
+    if (!pdl) {
+        tc_slot_persist_kernel<<<grid, kThreads, kSmemBytes, stream>>>(prm);
+        return launch_status();
+    }
+    return launch_pdl(tc_slot_persist_kernel, grid, kThreads, kSmemBytes, stream, prm);
+}
+
 }  // namespace
 
 bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == kD && a.scale > 0.f; }
+
+// The persistent kernel saves a fixed time at each unit boundary, but its tile loop runs a
+// little slower per key tile (more instruction-fetch and long-scoreboard stalls under ncu), so
+// it pays only for short units: at most 16 key tiles (measured against tc_attn_kernel, per
+// launch: 2 % faster at 11 tiles, 0.7 % slower at 21, 2.4 % at 35, 4-8 % at 68).  One wave or
+// less stays on tc_attn_kernel too: each CTA would take a single unit, and the fresh-CTA kernel
+// starts a little sooner and gives a lone query tile's split keys a third V stage.
+bool tc_slot_persistent(const AttnArgs& a, int B, int n_q, int T_len) {
+    const int64_t n_units = (int64_t)B * a.hq * (((int64_t)n_q + kQT * kBM - 1) / (kQT * kBM));
+    const int64_t n_kv = ((int64_t)T_len + kBN - 1) / kBN;
+    return tc_supported(a) && n_units > sm_count() && n_units < (1 << 22) && n_kv <= 16;
+}
 
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,
                              const int32_t* read_slot, const void* k_cache, const void* v_cache,
@@ -1366,8 +1970,9 @@ int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, i
     prm.T_len = T_len;
     prm.scale_log2 = a.scale * kLog2e;
     prm.budget = wait_budget();
-    return drop_none ? launch_attn<kSlotKeys, true>(prm, B, stream, pdl || chained)
-                     : launch_attn<kSlotKeys>(prm, B, stream, pdl || chained);
+    if (drop_none) return launch_attn<kSlotKeys, true>(prm, B, stream, pdl || chained);
+    if (out && tc_slot_persistent(a, B, n_q, T_len)) return launch_attn_persist(prm, B, stream, pdl || chained);
+    return launch_attn<kSlotKeys>(prm, B, stream, pdl || chained);
 }
 
 int launch_tc_slot_attention_varlen(const AttnArgs& a, int B, const int32_t* q_start, int max_q,

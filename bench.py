@@ -399,6 +399,8 @@ class Decode:
         # requests: the recompute kernel, whose lone query tile splits the keys over two chains)
         path = self.p.ac.acache_slot_attention_path(self.p.desc, w.batch, self.n, w.T)
         kernel, src = {self.p.ac._lib.ACACHE_PATH_RECOMPUTE: ("tc_attn_kernel (split keys)", "tc_attn.cu"),
+                       self.p.ac._lib.ACACHE_PATH_RECOMPUTE_PERSISTENT: ("tc_slot_persist_kernel (split keys)",
+                                                                        "tc_attn.cu"),
                        self.p.ac._lib.ACACHE_PATH_BLOCK_DECODE: ("tc_decode_kernel", "tc_decode.cu")}.get(
                            path, ("simt", None))
         return {

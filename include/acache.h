@@ -287,12 +287,20 @@ ACACHE_API int acache_slot_attention(const acache_attn_desc* a, int batch, int n
 /* Which kernel acache_slot_attention (and the attention of acache_store_attend) runs for a
  * geometry (host only, no GPU call): ACACHE_PATH_RECOMPUTE -- the tcgen05 kernel of two
  * 128-row query tiles per CTA (a lone tile splits its keys between two chains);
+ * ACACHE_PATH_RECOMPUTE_PERSISTENT -- the same computation in a persistent kernel (one CTA
+ * per SM working through the 256-row query blocks, its rings running on from one block into
+ * the next), chosen when there are more blocks than SMs and at most 16 key tiles (T <= 2048);
  * ACACHE_PATH_BLOCK_DECODE -- the tcgen05 kernel for few query rows per KV head, chosen when
  * it streams fewer K/V tiles (a GQA group's heads share one stream) or, with as many, when
  * the streams would leave most SMs idle and its cluster split of the keys fills them;
  * ACACHE_PATH_CUDA_CORES --
  * float32 or bf16 at d = 64.  Returns a negative status for invalid arguments. */
-enum { ACACHE_PATH_RECOMPUTE = 0, ACACHE_PATH_BLOCK_DECODE = 1, ACACHE_PATH_CUDA_CORES = 2 };
+enum {
+    ACACHE_PATH_RECOMPUTE = 0,
+    ACACHE_PATH_BLOCK_DECODE = 1,
+    ACACHE_PATH_CUDA_CORES = 2,
+    ACACHE_PATH_RECOMPUTE_PERSISTENT = 3
+};
 ACACHE_API int acache_slot_attention_path(const acache_attn_desc* a, int batch, int n_q, int seq_len);
 
 /* ---------------------------------------------------------------------------------

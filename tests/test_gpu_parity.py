@@ -319,17 +319,19 @@ def test_slot_attention_parity(dtype, d, heads, n_q, T):
     assert_out_close(out.float().cpu().numpy(), ref, dtype, "slot attention")
 
 
-# More CTAs (256-row query blocks of a request and head) than SMs, so the grid runs in several
-# waves, with GQA and MHA heads.  (B, n_q, Hq, Hkv, T): two-tile blocks followed by one-tile
-# blocks whose keys the two chains split; one key tile only (the one-tile blocks then have a
-# single chain); the fewest key tiles a split takes (2, 3); four to five waves; one-tile blocks
-# only.
+# More 256-row query blocks of a (request, head) than SMs: the persistent kernel, each CTA
+# working through several blocks, up to 16 key tiles; past that the fresh-CTA kernel in several
+# waves.  (B, n_q, Hq, Hkv, T): two-tile blocks followed by one-tile blocks whose keys the two
+# chains split; one key tile only (the one-tile blocks then have a single chain); the fewest
+# key tiles a split takes (2, 3); four to five blocks per CTA; one-tile blocks only; 17 key
+# tiles (the fresh-CTA kernel).
 WAVE_CASES = [
     (4, 600, 32, 8, 700),
     (4, 300, 32, 32, 100),
     (4, 300, 32, 4, 200),
     (2, 1100, 64, 8, 300),
     (8, 100, 32, 8, 500),
+    (2, 260, 64, 8, 2100),
 ]
 
 
