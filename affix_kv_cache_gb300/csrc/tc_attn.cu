@@ -59,7 +59,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <type_traits>
 
 #include "tc_attn.cuh"
 #include "ptx.cuh"
@@ -101,6 +100,21 @@ constexpr long long kLandBudget = 1LL << 21;      // cycles (~1 ms): TMA loads i
 
 enum KeyMode { kSlotKeys = 0, kProbeKeys = 1 };
 
+// n / d for 0 <= n < 2^31 and 1 <= d < 2^31 as one 64-bit multiply and a shift: with
+// l = ceil(log2 d), s = 32 + l and m = ceil(2^s / d), the excess e = m d - 2^s is below d <= 2^l,
+// so n e < 2^s and floor(n m / 2^s) = floor(n / d); n m < 2^64.
+struct FastDiv {
+    uint64_t m;
+    uint32_t s;
+    __host__ __device__ uint32_t operator()(uint32_t n) const { return (uint32_t)(((uint64_t)n * m) >> s); }
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint32_t s = 32 + l;
+    return FastDiv{((1ull << s) + d - 1) / d, s};
+}
+
 struct AttnParams {
     CUtensorMap tm_q;     // 4-D [B][n_rows][Hq][d], box {64, 1, 128, 1}
     CUtensorMap tm_k0;    // slot: 2-D pool [num_slots*Hkv][d], box {64, 1} (gather4)
@@ -125,7 +139,8 @@ struct AttnParams {
     int n_rows, Hq, Hkv, T_len, L, P;
     int g;                // Hq / Hkv
     int B;                // requests (persistent launch)
-    int n_kv, n_units;    // persistent launch: key tiles (<= 16), units (< 2^22)
+    int n_kv, n_units;    // persistent launch: key tiles (<= 20), units (< 2^22)
+    FastDiv div_bhq, div_hq, div_g;   // persistent launch: / (B Hq), / Hq, / (Hq / Hkv)
     float scale_log2;
     long long budget;     // cycles a pipeline wait may take before it gives up
 };
@@ -858,11 +873,10 @@ struct PUnit {
 };
 ACACHE_DEVFN PUnit punit(const AttnParams& p, int u, int n_kv) {
     PUnit w;
-    const int bhq = p.B * p.Hq;
-    const int qb = u / bhq, bh = u - qb * bhq;
-    w.b = bh / p.Hq;
+    const int qb = (int)p.div_bhq((uint32_t)u), bh = u - qb * p.B * p.Hq;
+    w.b = (int)p.div_hq((uint32_t)bh);
     w.h = bh - w.b * p.Hq;
-    w.hk = p.g == 1 ? w.h : w.h / p.g;
+    w.hk = (int)p.div_g((uint32_t)w.h);
     w.q0 = qb * kQT * kBM;
     w.n_qt = min(kQT, (p.n_rows - w.q0 + kBM - 1) / kBM);
     const bool split = w.n_qt == 1 && n_kv >= 2;
@@ -902,7 +916,7 @@ tc_slot_persist_kernel(const __grid_constant__ AttnParams p) {
     int raw0[4] = {-1, -1, -1, -1};
     uint32_t keys0 = 0;
     if (warp >= kMmaWarp + 2) {
-        const int b0 = (u_first % (p.B * p.Hq)) / p.Hq;
+        const int b0 = punit(p, u_first, n_kv).b;
         keys0 = tile_slots_load(p, (int64_t)b0 * p.T_len, p.T_len, n_kv, 0, lane, raw0);
     }
     if (threadIdx.x == 0) {
@@ -1033,116 +1047,115 @@ tc_slot_persist_kernel(const __grid_constant__ AttnParams p) {
             }
         } else {
             // ------------------------------------------------------------------ MMA issuers
-            // (as in tc_attn_kernel; chain t reads Q buffer t in every unit).  Compiled once per
-            // chain, so the chain's barriers, buffers and TMEM columns are constants.
-            auto mma_role = [&](auto chain) {
-                constexpr int t = decltype(chain)::value;
-                const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-                const uint32_t idO = idesc_bf16(kBM, kD, false, true);
-                const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
-                const uint64_t dq = sdesc_sw128(sQ(t), 16, 1024);
-                auto issue_s = [&](int eg) {
-                    const uint64_t dk = sdesc_sw128(sK(ring_stage(eg, kKStages)), 16, 1024);
+            // (as in tc_attn_kernel; chain t reads Q buffer t in every unit).  One body serves both
+            // chains: compiled once per chain it spilled nothing but ran slower, the larger code
+            // costing more instruction-fetch stalls than the spill.
+            {
+                const int t = warp - kMmaWarp;
+                if (lane == 0) {
+                    const uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+                    const uint32_t idO = idesc_bf16(kBM, kD, false, true);
+                    const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
+                    const uint64_t dq = sdesc_sw128(sQ(t), 16, 1024);
+                    auto issue_s = [&](int eg) {
+                        const uint64_t dk = sdesc_sw128(sK(ring_stage(eg, kKStages)), 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint64_t ko = ((uint64_t)(kk >> 2) * kRegion + (uint64_t)(kk & 3) * 32u) >> 4;
-                        umma_ss(d_s, dq + ko, dk + ko, idS, kk > 0);
-                    }
-                    umma_commit(&ctl.s_full[t]);
-                    umma_commit(&ctl.k_empty[ring_stage(eg, kKStages)]);
-                };
-                auto issue_pv_half = [&](int eg, bool acc, int hh) {
-                    const uint64_t dv = sdesc_sw128(sV(eg & 1), kRegion, 1024);
-#pragma unroll
-                    for (int kk = 4 * hh; kk < 4 * hh + 4; ++kk)
-                        umma_ts(d_o, d_s + kk * 8, dv + (uint64_t)(kk * 2048 / 16), idO, (acc || kk > 0));
-                };
-                // parity bit 0 counts this chain's tiles (P), bit 1 the units (Q); E the ring
-                // entries of the units before
-                uint32_t ph = 0;
-                int E = 0;
-                for (int u = u_first; u < n_units; u += u_step) {
-                    int nt, n0;
-                    bool split;
-                    {
-                        const PUnit w = punit(p, u, n_kv);
-                        nt = w.nt(t);
-                        n0 = w.ks.n0;
-                        split = w.ks.split;
-                    }
-                    // Entries this chain does not read are released once landed.  Unsplit units:
-                    // both chains read every entry (the idle chain of a one-tile unit, which then
-                    // has one key tile, reads none).  Split keys (KeySchedule): the entries alternate
-                    // chain A, chain B, chain A's extra tile (odd n_kv) last, so the entry before
-                    // each of this chain's own is the other chain's -- released (K before the S, V
-                    // before the PV) -- and so is the last entry if this chain does not own it.
-                    const int n1 = n_kv - n0;
-                    auto entry = [&](int i) { return split ? (i < n1 ? 2 * i + t : n1 + i) : i; };
-                    auto rel_k = [&](int eg) -> bool {
-                        if (!wait_bar(&ctl.k_full[ring_stage(eg, kKStages)], ring_lap(eg, kKStages) & 1, &ctl.abort,
-                                      p.dev_status, p.budget))
-                            return false;
-                        mbar_arrive(&ctl.k_empty[ring_stage(eg, kKStages)]);
-                        return true;
-                    };
-                    auto rel_v = [&](int eg) -> bool {
-                        if (!wait_bar(&ctl.v_full[eg & 1], (eg >> 1) & 1, &ctl.abort, p.dev_status, p.budget))
-                            return false;
-                        mbar_arrive(&ctl.v_empty[eg & 1]);
-                        return true;
-                    };
-                    bool ok = wait_bar(&ctl.q_full[t], (ph >> 1) & 1u, &ctl.abort, p.dev_status, p.budget);
-                    if (ok && nt > 0) {
-                        const int e0 = entry(0);
-                        ok = (!split || e0 == 0 || rel_k(E + e0 - 1)) &&
-                             wait_bar(&ctl.k_full[ring_stage(E + e0, kKStages)], ring_lap(E + e0, kKStages) & 1,
-                                      &ctl.abort, p.dev_status, p.budget);
-                        if (ok) {
-                            tc_fence_after();
-                            issue_s(E + e0);
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint64_t ko = ((uint64_t)(kk >> 2) * kRegion + (uint64_t)(kk & 3) * 32u) >> 4;
+                            umma_ss(d_s, dq + ko, dk + ko, idS, kk > 0);
                         }
-                        for (int i = 0; ok && i < nt; ++i) {
-                            const int e = entry(i), eg = E + e;
-                            const uint32_t pp = (ph ^ (uint32_t)i) & 1u;
-                            ok = (!split || e == 0 || rel_v(eg - 1)) &&
-                                 wait_bar(&ctl.v_full[eg & 1], (eg >> 1) & 1, &ctl.abort, p.dev_status, p.budget) &&
-                                 wait_bar(&ctl.p_half[t], pp, &ctl.abort, p.dev_status, p.budget);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_pv_half(eg, i > 0, 0);
-                            ok = wait_bar(&ctl.p_full[t], pp, &ctl.abort, p.dev_status, p.budget);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_pv_half(eg, i > 0, 1);
-                            umma_commit(&ctl.v_empty[eg & 1]);
-                            if (i + 1 < nt) {
-                                const int egn = E + entry(i + 1);
-                                ok = (!split || rel_k(egn - 1)) &&
-                                     wait_bar(&ctl.k_full[ring_stage(egn, kKStages)], ring_lap(egn, kKStages) & 1,
-                                              &ctl.abort, p.dev_status, p.budget);
+                        umma_commit(&ctl.s_full[t]);
+                        umma_commit(&ctl.k_empty[ring_stage(eg, kKStages)]);
+                    };
+                    auto issue_pv_half = [&](int eg, bool acc, int hh) {
+                        const uint64_t dv = sdesc_sw128(sV(eg & 1), kRegion, 1024);
+#pragma unroll
+                        for (int kk = 4 * hh; kk < 4 * hh + 4; ++kk)
+                            umma_ts(d_o, d_s + kk * 8, dv + (uint64_t)(kk * 2048 / 16), idO, (acc || kk > 0));
+                    };
+                    // parity bit 0 counts this chain's tiles (P), bit 1 the units (Q); E the ring
+                    // entries of the units before
+                    uint32_t ph = 0;
+                    int E = 0;
+                    for (int u = u_first; u < n_units; u += u_step) {
+                        int nt, n0;
+                        bool split;
+                        {
+                            const PUnit w = punit(p, u, n_kv);
+                            nt = w.nt(t);
+                            n0 = w.ks.n0;
+                            split = w.ks.split;
+                        }
+                        // Entries this chain does not read are released once landed.  Unsplit units:
+                        // both chains read every entry (the idle chain of a one-tile unit, which then
+                        // has one key tile, reads none).  Split keys (KeySchedule): the entries alternate
+                        // chain A, chain B, chain A's extra tile (odd n_kv) last, so the entry before
+                        // each of this chain's own is the other chain's -- released (K before the S, V
+                        // before the PV) -- and so is the last entry if this chain does not own it.
+                        const int n1 = n_kv - n0;
+                        auto entry = [&](int i) { return split ? (i < n1 ? 2 * i + t : n1 + i) : i; };
+                        auto rel_k = [&](int eg) -> bool {
+                            if (!wait_bar(&ctl.k_full[ring_stage(eg, kKStages)], ring_lap(eg, kKStages) & 1, &ctl.abort,
+                                          p.dev_status, p.budget))
+                                return false;
+                            mbar_arrive(&ctl.k_empty[ring_stage(eg, kKStages)]);
+                            return true;
+                        };
+                        auto rel_v = [&](int eg) -> bool {
+                            if (!wait_bar(&ctl.v_full[eg & 1], (eg >> 1) & 1, &ctl.abort, p.dev_status, p.budget))
+                                return false;
+                            mbar_arrive(&ctl.v_empty[eg & 1]);
+                            return true;
+                        };
+                        bool ok = wait_bar(&ctl.q_full[t], (ph >> 1) & 1u, &ctl.abort, p.dev_status, p.budget);
+                        if (ok && nt > 0) {
+                            const int e0 = entry(0);
+                            ok = (!split || e0 == 0 || rel_k(E + e0 - 1)) &&
+                                 wait_bar(&ctl.k_full[ring_stage(E + e0, kKStages)], ring_lap(E + e0, kKStages) & 1,
+                                          &ctl.abort, p.dev_status, p.budget);
+                            if (ok) {
+                                tc_fence_after();
+                                issue_s(E + e0);
+                            }
+                            for (int i = 0; ok && i < nt; ++i) {
+                                const int e = entry(i), eg = E + e;
+                                const uint32_t pp = (ph ^ (uint32_t)i) & 1u;
+                                ok = (!split || e == 0 || rel_v(eg - 1)) &&
+                                     wait_bar(&ctl.v_full[eg & 1], (eg >> 1) & 1, &ctl.abort, p.dev_status, p.budget) &&
+                                     wait_bar(&ctl.p_half[t], pp, &ctl.abort, p.dev_status, p.budget);
                                 if (!ok) break;
                                 tc_fence_after();
-                                issue_s(egn);
+                                issue_pv_half(eg, i > 0, 0);
+                                ok = wait_bar(&ctl.p_full[t], pp, &ctl.abort, p.dev_status, p.budget);
+                                if (!ok) break;
+                                tc_fence_after();
+                                issue_pv_half(eg, i > 0, 1);
+                                umma_commit(&ctl.v_empty[eg & 1]);
+                                if (i + 1 < nt) {
+                                    const int egn = E + entry(i + 1);
+                                    ok = (!split || rel_k(egn - 1)) &&
+                                         wait_bar(&ctl.k_full[ring_stage(egn, kKStages)], ring_lap(egn, kKStages) & 1,
+                                                  &ctl.abort, p.dev_status, p.budget);
+                                    if (!ok) break;
+                                    tc_fence_after();
+                                    issue_s(egn);
+                                }
                             }
+                            // split keys: the last entry, if the other chain's
+                            if (ok && split && ((n_kv & 1) == t)) ok = rel_k(E + n_kv - 1) && rel_v(E + n_kv - 1);
+                        } else if (ok) {
+                            // idle chain: every entry (one key tile)
+                            for (int e = 0; ok && e < n_kv; ++e) ok = rel_k(E + e) && rel_v(E + e);
                         }
-                        // split keys: the last entry, if the other chain's
-                        if (ok && split && ((n_kv & 1) == t)) ok = rel_k(E + n_kv - 1) && rel_v(E + n_kv - 1);
-                    } else if (ok) {
-                        // idle chain: every entry (one key tile)
-                        for (int e = 0; ok && e < n_kv; ++e) ok = rel_k(E + e) && rel_v(E + e);
+                        if (!ok) break;
+                        umma_commit(&ctl.drain[t]);
+                        E += n_kv;
+                        ph ^= (uint32_t)(nt & 1) | 2u;
                     }
-                    if (!ok) break;
-                    umma_commit(&ctl.drain[t]);
-                    E += n_kv;
-                    ph ^= (uint32_t)(nt & 1) | 2u;
+                    // no MMA may still run when TMEM is released
+                    umma_commit(&ctl.fin[t]);
+                    mbar_wait(&ctl.fin[t], 0, kDrainBudget);
                 }
-                // no MMA may still run when TMEM is released
-                umma_commit(&ctl.fin[t]);
-                mbar_wait(&ctl.fin[t], 0, kDrainBudget);
-            };
-            if (lane == 0) {
-                if (warp == kMmaWarp) mma_role(std::integral_constant<int, 0>{});
-                else mma_role(std::integral_constant<int, 1>{});
             }
             __syncwarp();
         }
@@ -1299,7 +1312,9 @@ tc_slot_persist_kernel(const __grid_constant__ AttnParams p) {
             if (writer && ok) {
                 tc_fence_after();
                 const float inv_l = 1.f / l_sum;
-#pragma unroll
+                // (not unrolled: it runs once per unit, and a smaller loop body keeps the
+                // instruction cache for the tile loop)
+#pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t o[32];
                     tmem_ld32(lane_base + col_o(t) + cc * 32, o);
@@ -1914,6 +1929,9 @@ int launch_attn_persist(AttnParams prm, int B, cudaStream_t stream, bool pdl) {
     prm.B = B;
     prm.n_kv = (prm.T_len + kBN - 1) / kBN;
     prm.n_units = (int)n_units;
+    prm.div_bhq = make_fastdiv((uint32_t)(B * prm.Hq));
+    prm.div_hq = make_fastdiv((uint32_t)prm.Hq);
+    prm.div_g = make_fastdiv((uint32_t)prm.g);
     const unsigned grid = (unsigned)std::min<int64_t>(n_units, sm_count());
     if (cudaFuncSetAttribute(tc_slot_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess) {
@@ -1932,15 +1950,15 @@ int launch_attn_persist(AttnParams prm, int B, cudaStream_t stream, bool pdl) {
 bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == kD && a.scale > 0.f; }
 
 // The persistent kernel saves a fixed time at each unit boundary, but its tile loop runs a
-// little slower per key tile (more instruction-fetch and long-scoreboard stalls under ncu), so
-// it pays only for short units: at most 16 key tiles (measured against tc_attn_kernel, per
-// launch: 2 % faster at 11 tiles, 0.7 % slower at 21, 2.4 % at 35, 4-8 % at 68).  One wave or
-// less stays on tc_attn_kernel too: each CTA would take a single unit, and the fresh-CTA kernel
-// starts a little sooner and gives a lone query tile's split keys a third V stage.
+// little slower per key tile (more instruction-fetch stalls under ncu), so it pays for short
+// units: at most 20 key tiles (measured against tc_attn_kernel per launch: 2-6 % faster at 11
+// tiles, 1.5 % at 17; even at 21 and 35; 1.5-2.3 % slower at 68).  One wave or less stays
+// on tc_attn_kernel too: each CTA would take a single unit, and the fresh-CTA kernel starts a
+// little sooner and gives a lone query tile's split keys a third V stage.
 bool tc_slot_persistent(const AttnArgs& a, int B, int n_q, int T_len) {
     const int64_t n_units = (int64_t)B * a.hq * (((int64_t)n_q + kQT * kBM - 1) / (kQT * kBM));
     const int64_t n_kv = ((int64_t)T_len + kBN - 1) / kBN;
-    return tc_supported(a) && n_units > sm_count() && n_units < (1 << 22) && n_kv <= 16;
+    return tc_supported(a) && n_units > sm_count() && n_units < (1 << 22) && n_kv <= 20;
 }
 
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,

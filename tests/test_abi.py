@@ -128,13 +128,13 @@ def test_slot_attention_path_choice():
     """Host-only: which kernel the read-slot attention picks for a geometry."""
     path = lambda hq, hkv, B, n_q, T, dt="bf16", d=128: ac.acache_slot_attention_path(  # noqa: E731
         ac.attn_desc(hq, hkv, d, d ** -0.5, dt), B, n_q, T)
-    # a recompute point: 384 blocks of 256 query rows (more than SMs) of 11 key tiles run
+    # a recompute point: 384 blocks of 256 query rows (more than SMs) of 11-20 key tiles run
     # persistent; 96 blocks, or 1,536 blocks of 35 key tiles, do not
     assert path(32, 32, 4, 589, 1408) == _lib.ACACHE_PATH_RECOMPUTE_PERSISTENT
     assert path(32, 32, 1, 589, 1408) == _lib.ACACHE_PATH_RECOMPUTE
     assert path(32, 32, 16, 1204, 4480) == _lib.ACACHE_PATH_RECOMPUTE
-    assert path(32, 32, 4, 589, 2048) == _lib.ACACHE_PATH_RECOMPUTE_PERSISTENT
-    assert path(32, 32, 4, 589, 2049) == _lib.ACACHE_PATH_RECOMPUTE
+    assert path(32, 32, 4, 589, 2560) == _lib.ACACHE_PATH_RECOMPUTE_PERSISTENT
+    assert path(32, 32, 4, 589, 2561) == _lib.ACACHE_PATH_RECOMPUTE
     assert path(32, 32, 4, 32, 1408) == _lib.ACACHE_PATH_RECOMPUTE       # decode, 128 streams
     assert path(32, 32, 1, 32, 1408) == _lib.ACACHE_PATH_BLOCK_DECODE    # decode, 32 streams
     assert path(28, 4, 16, 32, 2624) == _lib.ACACHE_PATH_BLOCK_DECODE    # GQA group shares a stream

@@ -320,11 +320,11 @@ def test_slot_attention_parity(dtype, d, heads, n_q, T):
 
 
 # More 256-row query blocks of a (request, head) than SMs: the persistent kernel, each CTA
-# working through several blocks, up to 16 key tiles; past that the fresh-CTA kernel in several
+# working through several blocks, up to 20 key tiles; past that the fresh-CTA kernel in several
 # waves.  (B, n_q, Hq, Hkv, T): two-tile blocks followed by one-tile blocks whose keys the two
 # chains split; one key tile only (the one-tile blocks then have a single chain); the fewest
 # key tiles a split takes (2, 3); four to five blocks per CTA; one-tile blocks only; 17 key
-# tiles (the fresh-CTA kernel).
+# tiles (still persistent); 21 key tiles (the fresh-CTA kernel).
 WAVE_CASES = [
     (4, 600, 32, 8, 700),
     (4, 300, 32, 32, 100),
@@ -332,6 +332,7 @@ WAVE_CASES = [
     (2, 1100, 64, 8, 300),
     (8, 100, 32, 8, 500),
     (2, 260, 64, 8, 2100),
+    (2, 260, 64, 8, 2600),
 ]
 
 
