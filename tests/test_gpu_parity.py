@@ -174,6 +174,24 @@ def test_probe_parity(layout, dtype, d, heads):
     assert_scores_close(scores.cpu().numpy(), ref["scores"], "probe scores")
 
 
+# More 256-row blocks of probe rows than SMs (4 requests x 32 query heads x 2 blocks = 256):
+# the forward runs in two waves, the last block of a (request, head) a one-tile block whose keys
+# the two chains split.  GQA (8 KV heads) and MHA; the affix as prefix and as infix.
+@pytest.mark.parametrize("layout,hkv", [("prefix", 8), ("infix", 32)])
+def test_probe_parity_more_blocks_than_sms(layout, hkv):
+    w = tiny(RAGGED[layout], hq=32, hkv=hkv, batch=4)
+    inp = wl.probe_inputs(w, 0)
+    ref = oracle.probe_layer(inp["q"], inp["k_req"], inp["v_req"], inp["k_aff"], inp["v_aff"],
+                             T=w.T, l=w.l, masked_rows=w.masked_rows(), scale=w.scale)
+    scores = torch.zeros((w.batch, w.L), dtype=torch.float32, device="cuda")
+    st = status_tensor()
+    o = probe_layer_gpu(w, inp, scores, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(o.float().cpu().numpy(), ref["out"], "bf16", "probe output")
+    assert_scores_close(scores.cpu().numpy(), ref["scores"], "probe scores")
+
+
 @pytest.mark.parametrize("m,consecutive", [(256, True), (257, True), (400, True), (200, False), (300, False)])
 def test_probe_parity_masked_row_counts(m, consecutive):
     """Up to 256 masked rows (two 128-row chunks) the masked-to-affix mass keeps them resident
