@@ -139,7 +139,7 @@ struct AttnParams {
     int n_rows, Hq, Hkv, T_len, L, P;
     int g;                // Hq / Hkv
     int B;                // requests (persistent launch)
-    int n_kv, n_units;    // persistent launch: key tiles (<= 20), units (< 2^22)
+    int n_kv, n_units;    // persistent launch: key tiles (< 2^15), units (< 2^22)
     FastDiv div_bhq, div_hq, div_g;   // persistent launch: / (B Hq), / Hq, / (Hq / Hkv)
     float scale_log2;
     long long budget;     // cycles a pipeline wait may take before it gives up
@@ -1949,16 +1949,19 @@ int launch_attn_persist(AttnParams prm, int B, cudaStream_t stream, bool pdl) {
 
 bool tc_supported(const AttnArgs& a) { return a.dtype == ACACHE_BF16 && a.d == kD && a.scale > 0.f; }
 
-// The persistent kernel saves a fixed time at each unit boundary, but its tile loop runs a
-// little slower per key tile (more instruction-fetch stalls under ncu), so it pays for short
-// units: at most 20 key tiles (measured against tc_attn_kernel per launch: 2-6 % faster at 11
-// tiles, 1.5 % at 17; even at 21 and 35; 1.5-2.3 % slower at 68).  One wave or less stays
-// on tc_attn_kernel too: each CTA would take a single unit, and the fresh-CTA kernel starts a
-// little sooner and gives a lone query tile's split keys a third V stage.
+// The persistent kernel saves a fixed time at each unit boundary.  With two query tiles per
+// unit its tile loop runs a little slower per key tile (more instruction-fetch stalls under
+// ncu), so there it pays for short units only: at most 20 key tiles (measured against
+// tc_attn_kernel per launch: 2-6 % faster at 11 tiles, 1.5 % at 17; even at 21 and 35; 1.5-2.3 %
+// slower at 68).  Units of one query tile (n_q <= 128: block decoding), whose keys the two chains
+// split, measured 1-2.5 % faster at every length tried (22, 35 and 68 key tiles).  One wave or
+// less stays on tc_attn_kernel: each CTA would take a single unit, and the fresh-CTA kernel
+// starts a little sooner and gives a lone query tile's split keys a third V stage.
 bool tc_slot_persistent(const AttnArgs& a, int B, int n_q, int T_len) {
     const int64_t n_units = (int64_t)B * a.hq * (((int64_t)n_q + kQT * kBM - 1) / (kQT * kBM));
     const int64_t n_kv = ((int64_t)T_len + kBN - 1) / kBN;
-    return tc_supported(a) && n_units > sm_count() && n_units < (1 << 22) && n_kv <= 20;
+    return tc_supported(a) && n_units > sm_count() && n_units < (1 << 22) && n_kv < (1 << 15) &&
+           (n_kv <= 20 || n_q <= kBM);
 }
 
 int launch_tc_slot_attention(const AttnArgs& a, int B, int n_q, const void* q, int T_len,

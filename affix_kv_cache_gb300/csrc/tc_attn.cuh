@@ -18,7 +18,8 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, i
 // True when the tcgen05 kernels cover this geometry (bf16, head_dim 128).
 bool tc_supported(const AttnArgs& a);
 // True when launch_tc_slot_attention (no discarded keys) runs the persistent kernel: more
-// 256-row query blocks of a (request, head) than SMs, within the kernel's counters.
+// 256-row query blocks of a (request, head) than SMs, and short units (at most 20 key tiles) or
+// one query tile per unit (at most 128 query rows).
 bool tc_slot_persistent(const AttnArgs& a, int B, int n_q, int T_len);
 
 // drop_none: read-slot entries equal to ACACHE_SLOT_NONE are discarded keys (DropNA).

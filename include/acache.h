@@ -289,7 +289,8 @@ ACACHE_API int acache_slot_attention(const acache_attn_desc* a, int batch, int n
  * 128-row query tiles per CTA (a lone tile splits its keys between two chains);
  * ACACHE_PATH_RECOMPUTE_PERSISTENT -- the same computation in a persistent kernel (one CTA
  * per SM working through the 256-row query blocks, its rings running on from one block into
- * the next), chosen when there are more blocks than SMs and at most 20 key tiles (T <= 2560);
+ * the next), chosen when there are more blocks than SMs and either at most 20 key tiles
+ * (T <= 2560) or at most 128 query rows (one query tile per block);
  * ACACHE_PATH_BLOCK_DECODE -- the tcgen05 kernel for few query rows per KV head, chosen when
  * it streams fewer K/V tiles (a GQA group's heads share one stream) or, with as many, when
  * the streams would leave most SMs idle and its cluster split of the keys fills them;

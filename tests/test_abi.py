@@ -133,6 +133,8 @@ def test_slot_attention_path_choice():
     assert path(32, 32, 4, 589, 1408) == _lib.ACACHE_PATH_RECOMPUTE_PERSISTENT
     assert path(32, 32, 1, 589, 1408) == _lib.ACACHE_PATH_RECOMPUTE
     assert path(32, 32, 16, 1204, 4480) == _lib.ACACHE_PATH_RECOMPUTE
+    assert path(32, 32, 16, 32, 4480) == _lib.ACACHE_PATH_RECOMPUTE_PERSISTENT   # 512 one-tile blocks
+    assert path(32, 32, 16, 129, 4480) == _lib.ACACHE_PATH_RECOMPUTE
     assert path(32, 32, 4, 589, 2560) == _lib.ACACHE_PATH_RECOMPUTE_PERSISTENT
     assert path(32, 32, 4, 589, 2561) == _lib.ACACHE_PATH_RECOMPUTE
     assert path(32, 32, 4, 32, 1408) == _lib.ACACHE_PATH_RECOMPUTE       # decode, 128 streams

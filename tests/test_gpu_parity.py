@@ -342,7 +342,8 @@ def test_slot_attention_parity(dtype, d, heads, n_q, T):
 # waves.  (B, n_q, Hq, Hkv, T): two-tile blocks followed by one-tile blocks whose keys the two
 # chains split; one key tile only (the one-tile blocks then have a single chain); the fewest
 # key tiles a split takes (2, 3); four to five blocks per CTA; one-tile blocks only; 17 key
-# tiles (still persistent); 21 key tiles (the fresh-CTA kernel).
+# tiles (still persistent); 21 key tiles (the fresh-CTA kernel); one-tile blocks of 22 key
+# tiles (persistent: with one query tile per block there is no key-tile limit).
 WAVE_CASES = [
     (4, 600, 32, 8, 700),
     (4, 300, 32, 32, 100),
@@ -351,6 +352,7 @@ WAVE_CASES = [
     (8, 100, 32, 8, 500),
     (2, 260, 64, 8, 2100),
     (2, 260, 64, 8, 2600),
+    (6, 40, 32, 8, 2700),
 ]
 
 
