@@ -31,6 +31,18 @@ def test_library_exports_every_declared_symbol():
     assert ac.status_string(0) == "ok"
 
 
+def test_binding_constants_match_header():
+    """Every ACACHE_* enumerator and #define of the header has the same value in the binding
+    (status codes, dtypes, device-status bits, kernel paths, the discarded-key sentinel)."""
+    src = open(HEADER).read()
+    found = dict((n, int(v)) for n, v in re.findall(r"\b(ACACHE_[A-Z0-9_]+)\s*=\s*(-?\d+)", src))
+    found.update((n, int(v)) for n, v in re.findall(r"#define\s+(ACACHE_[A-Z0-9_]+)\s+\((-?\d+)\)", src))
+    assert len(found) >= 20, sorted(found)
+    for name, value in found.items():
+        py = name if hasattr(_lib, name) else name.replace("ACACHE_", "", 1)
+        assert getattr(_lib, py) == value, (name, getattr(_lib, py), value)
+
+
 def test_wait_budget_set_and_read_on_the_host():
     # host-side state only: no kernel is launched
     default = ac.acache_wait_budget()
